@@ -1,0 +1,440 @@
+"""Benchmark of the W4A16 group-wise linear layer on GB300.
+
+Workload (one step): a decode token through the linears of a stack of 8 decoder layers of the
+pages' model -- q_k_v (K=2048, N=3072), gate_up (K=2048, N=13312), down (K=6656, N=2048), group
+g=128, M=1 row of x -- each layer with its own weights (8 x 24.6 MB = 197 MB of packed weights
+per step, more than the 129 MB L2, so every step streams its weights from HBM).  The step is
+captured once in a CUDA graph and replayed.
+
+Metric: effective HBM GB/s at M=1 = algorithmic bytes / time, algorithmic bytes per linear =
+K*N/2 (codes) + (K/g)*N*(0.5 + 2) (zeros, scales) + 2*M*K (x) + 2*M*N (y).  A secondary block
+reports the M=512 prefill shapes in TFLOP/s (2*M*N*K per linear).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the layer does not
+shard across GPUs here: "replicas only"); value = all ranks' bytes / the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a16_group_wise_gb300 import inputs  # noqa: E402
+
+G = 128
+DECODE_SHAPES = [("qkv", 2048, 3072), ("gate_up", 2048, 13312), ("down", 6656, 2048)]
+LAYERS = 8
+METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate_up/down, g=128)"
+
+# DRAM bytes per launch of the decode kernel from the ncu capture summarised in
+# profiles/gemv_decode_ncu.md, keyed by the sha256 of the kernel source it was taken on; it
+# is reported as null whenever the source has changed since.
+TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+
+
+def alg_bytes(M, K, N, g=G):
+    return K * N // 2 + (K // g) * N * 5 // 2 + 2 * M * K + 2 * M * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ------------------------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import w4a16_group_wise_gb300 as w4
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+
+    # ---------------- resident weights: LAYERS copies of the three decoder linears
+    layers = []
+    with torch.cuda.stream(stream):
+        for li in range(LAYERS):
+            lin = []
+            for name, K, N in DECODE_SHAPES:
+                h = inputs.make_weights(K, N, G, seed=1000 * rank + 10 * li + len(lin))
+                qw = torch.from_numpy(h["qweight"]).to(dev)
+                qz = torch.from_numpy(h["qzeros"]).to(dev)
+                sc = torch.from_numpy(h["scales"]).to(dev)
+                packed = w4.repack(qw, qz, sc, K, N, G, stream=stream)
+                lin.append((name, K, N, packed))
+                del qw, qz, sc
+            layers.append(lin)
+    stream.synchronize()
+
+    M = 1
+    launches = [(li, name, K, N, packed) for li, lin in enumerate(layers) for (name, K, N, packed) in lin]
+    xs = [torch.from_numpy(inputs.make_x(M, K, seed=i)).to(dev) for i, (_, _, K, _, _) in enumerate(launches)]
+    ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for (_, _, _, N, _) in launches]
+    step_bytes = sum(alg_bytes(M, K, N) for (_, _, K, N, _) in launches)
+
+    def step():
+        for (_, _, K, N, packed), x, y in zip(launches, xs, ys):
+            w4.gemm(x, packed, M, N, K, G, y=y, stream=stream)
+
+    # warm up eagerly (also the correctness-relevant first launches), then capture the step
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if w4.last_device_error(stream) != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    def timed(fn, steps):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def replay():
+        with torch.cuda.stream(stream):
+            graph.replay()
+
+    with ClockSampler(local_rank) as clk:
+        ms = timed(replay, args.steps)
+    ms_step = ms / args.steps
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+
+    # ---------------- per-shape kernel times (8 launches of one shape per graph replay)
+    per_shape = {}
+    for name, K, N in DECODE_SHAPES:
+        sel = [(l, x, y) for l, x, y in zip(launches, xs, ys) if l[1] == name]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            for (_, _, k_, n_, packed), x, y in sel:
+                w4.gemm(x, packed, M, n_, k_, G, y=y, stream=stream)
+        for _ in range(3):
+            g2.replay()
+        reps = min(2000, max(20, args.steps))
+
+        def rep():
+            with torch.cuda.stream(stream):
+                g2.replay()
+        t = timed(rep, reps) / (reps * len(sel))
+        b = alg_bytes(M, K, N)
+        per_shape[name] = {"K": K, "N": N, "us_per_launch": round(t * 1e3, 3),
+                           "gbs": round(b / (t * 1e-3) / 1e9, 1), "frac": round(b / (t * 1e-3) / 1e9 / hbm, 3)}
+
+    # ---------------- e2e: host x in, host y out, through the public API, per step
+    x_host = torch.empty(sum(x.numel() for x in xs), dtype=torch.float16).pin_memory()
+    y_host = torch.empty(sum(y.numel() for y in ys), dtype=torch.float16).pin_memory()
+    off = 0
+    for x in xs:
+        x_host[off:off + x.numel()].copy_(x.view(-1).cpu())
+        off += x.numel()
+    x_dev = torch.empty_like(x_host, device=dev)
+    y_dev = torch.empty_like(y_host, device=dev)
+    xv, yv, ox, oy = [], [], 0, 0
+    for (_, _, K, N, _) in launches:
+        xv.append(x_dev[ox:ox + M * K].view(M, K))
+        yv.append(y_dev[oy:oy + M * N].view(M, N))
+        ox += M * K
+        oy += M * N
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            for (_, _, K, N, packed), x, y in zip(launches, xv, yv):
+                w4.gemm(x, packed, M, N, K, G, y=y, stream=stream)
+            y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps) / args.steps
+    e2e = {"value": round(step_bytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+           "ms_per_step": round(ms_e2e, 4)}
+
+    # ---------------- prefill M=512 (secondary): TFLOP/s of the three shapes
+    prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
+
+    gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
+    traffic = None
+    if TRAFFIC["source_sha256"] == source_sha(gemv_src) and TRAFFIC["bytes_per_launch"]:
+        traffic = TRAFFIC["bytes_per_launch"]
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9   # all launches of the step are this kernel
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; AWQ codes uniform 0..15, scales U[0.002,0.02] fp16, x N(0,1) fp16)",
+        "config": workload_config(len(launches), sum(p.numel() for (_, _, _, _, p) in launches) / 1e6, world),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "kernel": "gemv_kernel (decode)", "peak_source": peak_src,
+                     "note": "achieved = algorithmic bytes of the step / step time; every launch of the step is the decode kernel"},
+        "per_shape": per_shape,
+        "prefill": prefill,
+        "e2e": e2e,
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clk.summary(),
+    }
+    return result
+
+
+def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src):
+    M = 512
+    out = {}
+    tot_flops, tot_ms = 0.0, 0.0
+    for si, (name, K, N) in enumerate(DECODE_SHAPES):
+        x = torch.from_numpy(inputs.make_x(M, K, seed=77)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        sel = [lin[si][3] for lin in layers]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for p in sel:
+                w4.gemm(x, p, M, N, K, G, y=y, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g2, stream=stream):
+            for p in sel:
+                w4.gemm(x, p, M, N, K, G, y=y, stream=stream)
+        for _ in range(3):
+            g2.replay()
+        reps = min(200, max(5, args.steps // 4))
+
+        def rep():
+            with torch.cuda.stream(stream):
+                g2.replay()
+        ms = timed(rep, reps) / (reps * len(sel))
+        fl = 2.0 * M * N * K
+        out[name] = {"K": K, "N": N, "M": M, "us_per_launch": round(ms * 1e3, 2),
+                     "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
+        tot_flops += fl
+        tot_ms += ms
+    tf = tot_flops / (tot_ms * 1e-3) / 1e12
+    out["all"] = {"metric": "TFLOP/s at M=512 (q_k_v, gate_up, down; fp16 x fp16 -> fp32)",
+                  "value": round(tf, 1), "unit": "TFLOP/s",
+                  "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16, "unit": "TFLOP/s",
+                               "frac": round(tf / bf16, 4), "peak_source": peak_src + " (bf16 burst; fp16 dense rate is the same)"}}
+    return out
+
+
+# -------------------------------------------------------------------------------- reference
+
+def _oracle_layer(cols=None):
+    """One decoder layer's three linears at M=1, optionally only their first `cols` columns."""
+    layer = []
+    for i, (name, K, N) in enumerate(DECODE_SHAPES):
+        n = N if cols is None else min(N, cols)
+        h = inputs.make_weights(K, n, G, seed=i)
+        layer.append((K, n, h, inputs.make_x(1, K, seed=i)))
+    return layer
+
+
+def _oracle_pass(layer):
+    import oracle
+    for K, N, h, x in layer:
+        oracle.linear(x.view(np.uint16), h["qweight"], h["qzeros"], h["scales"].view(np.uint16), K, N, G)
+
+
+def oracle_sample(budget_s=10.0):
+    """Time the CPU oracle, as it stands, on one decoder layer's three linears at M=1."""
+    import oracle
+
+    layer = _oracle_layer()
+    sample_bytes = sum(alg_bytes(1, K, N) for (K, N, _, _) in layer)
+    t0 = time.perf_counter()
+    _oracle_pass(layer)
+    t1 = time.perf_counter() - t0
+    reps = max(1, int(np.ceil(budget_s / max(t1, 1e-3))) - 1)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_pass(layer)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(sample_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "one decoder layer's q_k_v, gate_up, down at M=1 (%.1f MB algorithmic), %d timed passes "
+                      "of %.3f s" % (sample_bytes / 1e6, reps, dt)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one pass over a column slice of one decoder
+    layer's three linears at M=1, the slice sized so the whole run takes about two minutes."""
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build.build()
+    full = _oracle_layer()
+    t0 = time.perf_counter()
+    _oracle_pass(full)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, 120.0 / ((args.steps + args.warmup) * max(t_full, 1e-6)))
+    cols = max(64, int(frac * 13312) // 64 * 64)
+    layer = _oracle_layer(cols) if cols < 13312 else full
+    step_bytes = sum(alg_bytes(1, K, N) for (K, N, _, _) in layer)
+    for _ in range(args.warmup):
+        _oracle_pass(layer)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_pass(layer)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = step_bytes / dt / 1e9
+    sample = ("per step: the first %d columns of each of one decoder layer's q_k_v, gate_up, down at M=1 "
+              "(%.2f MB algorithmic)" % (cols, step_bytes / 1e6))
+    cfg = workload_config()
+    cfg["sample"] = sample
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def workload_config(n_launches=3 * LAYERS, packed_mb=None, world=1):
+    cfg = {"workload": "decode token through %d decoder layers' linears: q_k_v 2048x3072, gate_up 2048x13312, "
+                       "down 6656x2048 (KxN), g=128, M=1; %d gemm launches per step" % (LAYERS, n_launches),
+           "l2": "inputs larger than L2 (%s MB packed weights per step, distinct per layer)"
+                 % ("%.1f" % packed_mb if packed_mb else "197"),
+           "graph": "step captured once in a CUDA graph and replayed",
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    return cfg
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            cb = oracle_sample()
+            cb.pop("seconds_per_pass", None)
+            res["cpu_baseline"] = cb
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

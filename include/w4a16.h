@@ -1,0 +1,138 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) asymmetric group-wise W4A16 linear layer.
+ *
+ *   y[M,N] = x[M,K] . W,   W[k,n] = (q[k,n] - z[k/g,n]) * s[k/g,n]
+ *
+ * q and z are 4-bit codes (0..15) packed eight to an int32 along N in the AWQ checkpoint order,
+ * s is fp16, x and y are fp16, and one group covers g consecutive rows of K.
+ *
+ * Where the operations come from:
+ *  - "Carga de capas cuantizadas: AWQ / GPTQ / Marlin / fp8" (vLLM architecture walkthrough):
+ *    section "Responsabilidades" splits a quantized linear into create_weights, a one-time
+ *    process_weights_after_loading reorder, and apply (the GEMM); w4a16_repack is the one-time
+ *    reorder and w4a16_gemm is apply.  Section "Flujo de datos" gives the tensors w4a16_repack
+ *    takes: qweight int32 [K, N/8], qzeros int32 [K/g, N/8] (both packed along the output
+ *    dimension) and scales [K/g, N].  Section "Limites y fallos" (verify_marlin_supported)
+ *    rejects unsupported group sizes and types with an error: here, a status code.
+ *  - vllm-omni commit "Add cpu_int4, an asymmetric 4-bit weight path for vLLM's CPU backend":
+ *    the asymmetric grid, and the two paths over one set of weights (a decode path for few
+ *    rows, a dense path for many), which w4a16_gemm picks between by M.
+ *  - vllm-omni commit "cpu_int4: dequantize prefill weights from the tinygemm layout, not a
+ *    copy": the packed layout need not be opaque; decoding it back is w4a16_dequant, which is
+ *    bit-exact against the straightforward dequantizer.  The N = 80 case (64 + a 16 tail) must
+ *    be handled, not misread.
+ *  - vllm-omni commit "cpu_int4: repack weights in n-blocks, to bound the load-time peak":
+ *    n-blocks are independent, so w4a16_repack_chunk packs one n-range at a time and gives the
+ *    same bytes as packing the whole matrix.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing and keeps no pointer after the call returns.  Every call is asynchronous and
+ *    ordered on `stream` (a cudaStream_t; NULL means the legacy default stream).  Apart from
+ *    w4a16_last_device_error, no call synchronizes.
+ *  - Shapes are int; K, N, g > 0.  Supported: g in {32, 64, 128}, K % g == 0, N % 8 == 0.
+ *    N need not be a multiple of 64 and K need not be a multiple of 128.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Return value: W4A16_OK or a negative status (below).  No C++ exception crosses the ABI.
+ *    A status other than W4A16_OK means nothing was launched.  Errors raised on the device
+ *    (a packed buffer whose header does not match the call's K, N, g, or a bounded wait that
+ *    ran out) are recorded in a per-device error word read by w4a16_last_device_error.
+ */
+#ifndef W4A16_GB300_H
+#define W4A16_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define W4A16_OK 0
+#define W4A16_ERR_INVALID (-1)     /* null pointer, K/N/g <= 0, M < 0, bad n-range          */
+#define W4A16_ERR_UNSUPPORTED (-2) /* N % 8 != 0, K % g != 0, g not in {32, 64, 128}         */
+#define W4A16_ERR_MISALIGNED (-3)  /* a device pointer is not 16-byte aligned                */
+#define W4A16_ERR_WORKSPACE (-4)   /* workspace smaller than w4a16_workspace_bytes           */
+#define W4A16_ERR_CUDA (-5)        /* a CUDA call or kernel launch failed                    */
+#define W4A16_ERR_DEVICE (-6)      /* device-side error, reported by w4a16_last_device_error */
+
+/* Version of the packed layout written by w4a16_repack; stored in every packed buffer's
+ * header and checked on the device by w4a16_gemm and w4a16_dequant. */
+#define W4A16_LAYOUT_VERSION 1
+
+/*
+ * Packed layout, version 1 (own design; the layouts of the pages' other kernels are prior
+ * art).  All offsets in bytes from the start of the buffer.
+ *   [0, 256)      header: uint32 magic 0x36314134, uint32 version, int32 K, int32 N, int32 g,
+ *                 then zeros.
+ *   [256, ...)    NB = ceil(N/64) n-blocks, each of KT = ceil(K/128) chunks of
+ *                 CB = 4096 + (128/g) * 160 bytes; chunk (b, t) starts at 256 + (b*KT + t)*CB
+ *                 and covers columns [64b, 64b+64) and rows k in [128t, 128t+128).
+ *   chunk codes   [0, 4096): 64 column-rows of 64 bytes; row r is column n = 64b + r and holds
+ *                 128 consecutive k as 16 little-endian uint32 words.  Word w holds
+ *                 k = 128t + 8w + {0,2,4,6,1,3,5,7}[j] in nibble slot j (bits 4j..4j+3).
+ *   chunk meta    [4096, CB): for each of the 128/g groups l of the chunk, 160 bytes:
+ *                 64 fp16 scales then 32 bytes of zero codes, both in "lane order": position
+ *                 p = 8*(r%8) + 2*(r/16) + (r/8)%2 holds column-row r; the zero of position p
+ *                 is nibble p%8 (bits 4(p%8)..) of little-endian uint32 word p/8.
+ *   padding       columns n >= N and rows k >= K have code 0, zero code 0 and scale +0.0, so
+ *                 the buffer's bytes are a pure function of (qweight, qzeros, scales, K, N, g).
+ */
+
+/* Bytes of the packed buffer for a K x N layer with group size g; 0 if the shape is invalid
+ * or unsupported. */
+size_t w4a16_packed_bytes(int K, int N, int g);
+
+/* Bytes of device workspace w4a16_gemm needs for this problem; 0 means none (workspace may
+ * then be NULL).  Stable for given arguments. */
+size_t w4a16_workspace_bytes(int M, int N, int K, int g);
+
+/* One-time repack of AWQ tensors into the packed layout (integer-exact; scales copied bit for
+ * bit).  qweight int32 [K][N/8], qzeros int32 [K/g][N/8], scales fp16 bits [K/g][N], all
+ * row-major and contiguous; packed: w4a16_packed_bytes(K, N, g) bytes, fully written. */
+int w4a16_repack(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                 int K, int N, int g, void *packed, void *stream);
+
+/* Repack only columns [n0, n1) into their n-blocks of `packed` (and the header).  n0 must be
+ * a multiple of 64; n1 a multiple of 64 or equal to N; 0 <= n0 < n1 <= N.  The inputs are the
+ * slices starting at column n0: qweight_c points at qweight[0][n0/8] with a row stride of
+ * ld_qweight int32 elements, qzeros_c at qzeros[0][n0/8] (stride ld_qzeros), scales_c at
+ * scales[0][n0] (stride ld_scales fp16 elements); a caller that holds only the slice passes
+ * its compact strides.  Repacking every n-range of a partition of [0, N) yields the same
+ * bytes as w4a16_repack. */
+int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight,
+                       const int32_t *qzeros_c, int64_t ld_qzeros,
+                       const uint16_t *scales_c, int64_t ld_scales,
+                       int K, int N, int g, int n0, int n1, void *packed, void *stream);
+
+/* y = x . W.  x fp16 bits [M][K] row-major, y fp16 bits [M][N] row-major (fully written),
+ * packed from w4a16_repack with the same K, N, g.  M == 0 is a no-op.  M <= 16 takes the
+ * decode path (fused dequant + skinny GEMM streaming the packed weights once); larger M the
+ * tensor-core path.  Accumulation is in fp32; the result is rounded once to fp16 and is
+ * bit-identical from run to run.  workspace: w4a16_workspace_bytes(M, N, K, g) bytes of device
+ * memory (may be NULL when that is 0). */
+int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/* W = fp16((q - z) * s) for every k < K, n < N, written as fp16 bits [K][N] row-major: one
+ * round-to-nearest-even rounding of the exact product, bit-identical to the straightforward
+ * dequantizer. */
+int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream);
+
+/* Static description of a status code. */
+const char *w4a16_status_string(int status);
+
+/* Synchronizes `stream`, then returns W4A16_ERR_DEVICE if a kernel of this library recorded a
+ * device-side error on the current device since the last call (and clears the record),
+ * W4A16_ERR_CUDA if the synchronization itself failed, else W4A16_OK. */
+int w4a16_last_device_error(void *stream);
+
+/* W4A16_LAYOUT_VERSION of the library actually loaded. */
+int w4a16_layout_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_GB300_H */

@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every entry point include/w4a16.h declares, and rejects bad
+arguments on the host (these calls return before any CUDA call, so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from w4a16_group_wise_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return binding.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "w4a16_gemm" in names and "w4a16_repack" in names and "w4a16_dequant" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) <= set(binding.SIGNATURES)
+
+
+def test_exports_nothing_undeclared():
+    out = os.popen("nm -D --defined-only %s" % binding.LIB_PATH).read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and "w4a16" in l}
+    assert exported == set(_declared())
+
+
+def test_layout_version_and_sizes(L):
+    assert L.w4a16_layout_version() == 1
+    # 256-byte header + ceil(N/64) * ceil(K/128) chunks of 4096 + (128/g) * 160 bytes
+    assert L.w4a16_packed_bytes(2048, 13312, 128) == 256 + 208 * 16 * 4256
+    assert L.w4a16_packed_bytes(6656, 80, 32) == 256 + 2 * 52 * (4096 + 4 * 160)
+    assert L.w4a16_packed_bytes(96, 8, 32) == 256 + 1 * 1 * 4736
+    assert L.w4a16_packed_bytes(2048, 2048, 100) == 0
+    assert L.w4a16_packed_bytes(2048, 2044, 128) == 0
+    assert L.w4a16_packed_bytes(2000, 2048, 128) == 0
+    assert L.w4a16_packed_bytes(0, 2048, 128) == 0
+    assert L.w4a16_workspace_bytes(1, 2048, 2048, 128) == 0
+
+
+P = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: every case below fails first
+P_ODD = ctypes.c_void_p(0x10008)
+NUL = ctypes.c_void_p(0)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((P, P, 1, 2048, 2048, 100, P, NUL, 0, NUL), binding.ERR_UNSUPPORTED),   # g
+    ((P, P, 1, 2044, 2048, 128, P, NUL, 0, NUL), binding.ERR_UNSUPPORTED),   # N % 8
+    ((P, P, 1, 2048, 2000, 128, P, NUL, 0, NUL), binding.ERR_UNSUPPORTED),   # K % g
+    ((P, P, -1, 2048, 2048, 128, P, NUL, 0, NUL), binding.ERR_INVALID),      # M < 0
+    ((P, P, 1, 0, 2048, 128, P, NUL, 0, NUL), binding.ERR_INVALID),          # N = 0
+    ((NUL, P, 1, 2048, 2048, 128, P, NUL, 0, NUL), binding.ERR_INVALID),     # x null
+    ((P, NUL, 1, 2048, 2048, 128, P, NUL, 0, NUL), binding.ERR_INVALID),     # packed null
+    ((P, P, 1, 2048, 2048, 128, NUL, NUL, 0, NUL), binding.ERR_INVALID),     # y null
+    ((P_ODD, P, 1, 2048, 2048, 128, P, NUL, 0, NUL), binding.ERR_MISALIGNED),
+    ((P, P, 1, 2048, 2048, 128, P_ODD, NUL, 0, NUL), binding.ERR_MISALIGNED),
+    ((P, P, 0, 2048, 2048, 128, NUL, NUL, 0, NUL), binding.OK),              # M = 0: no-op
+])
+def test_gemm_host_validation(L, args, status):
+    assert L.w4a16_gemm(*args) == status
+
+
+def test_repack_and_dequant_host_validation(L):
+    assert L.w4a16_repack(P, P, P, 2048, 2048, 96, P, NUL) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_repack(NUL, P, P, 2048, 2048, 128, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_repack(P, P, P, 2048, 2048, 128, P_ODD, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_dequant(P, 2048, 2048, 64, NUL, NUL) == binding.ERR_INVALID
+    assert L.w4a16_dequant(P, 2048, 2050, 64, P, NUL) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_dequant(P_ODD, 2048, 2048, 64, P, NUL) == binding.ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("n0,n1", [(32, 128), (0, 100), (128, 64), (0, 0), (-64, 64), (0, 2112)])
+def test_repack_chunk_rejects_bad_ranges(L, n0, n1):
+    # N = 2048: n0 must be a multiple of 64, n1 a multiple of 64 or N, 0 <= n0 < n1 <= N
+    st = L.w4a16_repack_chunk(P, 256, P, 256, P, 2048, 2048, 2048, 128, n0, n1, P, NUL)
+    assert st == binding.ERR_INVALID
+
+
+def test_repack_chunk_rejects_short_strides(L):
+    assert L.w4a16_repack_chunk(P, 7, P, 8, P, 64, 2048, 2048, 128, 0, 64, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_repack_chunk(P, 8, P, 8, P, 63, 2048, 2048, 128, 0, 64, P, NUL) == binding.ERR_INVALID
+
+
+def test_status_strings(L):
+    for s in range(-6, 1):
+        assert binding.status_string(s) and "unknown" not in binding.status_string(s)
+    assert "unknown" in binding.status_string(-99)

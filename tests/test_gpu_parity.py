@@ -1,0 +1,287 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Bars: repack and dequant bit-exact; GEMM within max|y - y_ref| <= 2e-2 * rms(y_ref) and mean
+relative error <= 5e-3 (y_ref = fp64 oracle rounded to fp16), bit-exact where every partial sum
+is exact, run-to-run bit-identical, and no write outside the output.
+"""
+import numpy as np
+import pytest
+
+from gpu_util import Layer, assert_close, awq_column_slice, dev, errors, torch
+import oracle
+import w4a16_group_wise_gb300 as w4
+from w4a16_group_wise_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = inputs.SHAPES
+SLOT_K = [0, 2, 4, 6, 1, 3, 5, 7]
+
+
+# ------------------------------------------------------------------ dequant: bit-exact
+
+@pytest.mark.parametrize("K,N,g", [
+    (256, 128, 128), (96, 80, 32), (192, 8, 64), (384, 136, 32),
+    (6656, 80, 32), (6656, 80, 64), (6656, 80, 128),
+    (2048, 2048, 128), (2048, 3072, 128), (2048, 13312, 128), (6656, 2048, 128),
+])
+def test_dequant_bit_exact(K, N, g):
+    L = Layer(K, N, g, seed=K + N + g)
+    W = w4.dequant(L.packed, K, N, g)
+    ref = oracle.dequant_f16_bits(L.qweight, L.qzeros, L.scales_bits, K, N, g)
+    assert np.array_equal(W.cpu().numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("zeros", ["sym8", "uniform"])
+def test_dequant_bit_exact_edge_distributions(g, zeros):
+    K, N = 6656, 80
+    L = Layer(K, N, g, seed=5, zeros=zeros, scale_dist="loguniform", scale_lo=1e-4, scale_hi=0.1)
+    W = w4.dequant(L.packed, K, N, g)
+    ref = oracle.dequant_f16_bits(L.qweight, L.qzeros, L.scales_bits, K, N, g)
+    assert np.array_equal(W.cpu().numpy().view(np.uint16), ref)
+
+
+def test_dequant_lm_head_sampled_columns():
+    K, N = SHAPES["lm_head"]
+    L = Layer(K, N, 128, seed=3)
+    W = w4.dequant(L.packed, K, N, 128)
+    for n0 in (0, 65536, N - 512):
+        qw, qz, s = awq_column_slice(L, n0, n0 + 512)
+        ref = oracle.dequant_f16_bits(qw, qz, s, K, 512, 128)
+        assert np.array_equal(W[:, n0:n0 + 512].cpu().numpy().view(np.uint16), ref)
+
+
+def test_dequant_guard_bands():
+    K, N, g = 384, 80, 64
+    L = Layer(K, N, g, seed=1)
+    buf = torch.full((K * N + 4096,), -7.0, dtype=torch.float16, device=dev())
+    out = buf[2048:2048 + K * N].view(K, N)
+    w4.dequant(L.packed, K, N, g, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:2048] == -7.0) and torch.all(buf[2048 + K * N:] == -7.0)
+
+
+# ------------------------------------------------------------------ repack: the bytes themselves
+
+def _decode_packed(buf, K, N, g):
+    """Read the packed layout version 1 back by its written specification (include/w4a16.h)."""
+    hdr = buf[:20].view(np.uint32)
+    NB, KT = -(-N // 64), -(-K // 128)
+    gpc = 128 // g
+    CB = 4096 + gpc * 160
+    body = buf[256:256 + NB * KT * CB].reshape(NB, KT, CB)
+    words = np.ascontiguousarray(body[:, :, :4096]).view(np.uint32).reshape(NB, KT, 64, 16)
+    q = np.zeros((KT * 128, NB * 64), np.uint8)
+    for j in range(8):
+        nib = ((words >> (4 * j)) & 0xF).astype(np.uint8)          # [b, t, r, w]
+        for t in range(KT):
+            for w in range(16):
+                q[128 * t + 8 * w + SLOT_K[j], :] = nib[:, t, :, w].reshape(-1)
+    meta = np.ascontiguousarray(body[:, :, 4096:]).reshape(NB, KT, gpc, 160)
+    sc = np.ascontiguousarray(meta[..., :128]).view(np.uint16)     # [b, t, l, p]
+    zw = np.ascontiguousarray(meta[..., 128:]).view(np.uint32)     # [b, t, l, word]
+    s = np.zeros((KT * gpc, NB * 64), np.uint16)
+    z = np.zeros((KT * gpc, NB * 64), np.uint8)
+    for p in range(64):
+        r = 16 * ((p % 8) // 2) + 8 * (p % 2) + p // 8
+        for t in range(KT):
+            for l in range(gpc):
+                s[t * gpc + l, r::64] = sc[:, t, l, p]
+                z[t * gpc + l, r::64] = (zw[:, t, l, p // 8] >> (4 * (p % 8))) & 0xF
+    return hdr, q, s, z
+
+
+@pytest.mark.parametrize("K,N,g", [(384, 80, 64), (256, 136, 128), (96, 72, 32)])
+def test_repack_bytes_follow_documented_layout(K, N, g):
+    L = Layer(K, N, g, seed=2)
+    buf = L.packed.cpu().numpy()
+    assert buf.size == w4.packed_bytes(K, N, g)
+    hdr, q, s, z = _decode_packed(buf, K, N, g)
+    assert hdr.tolist() == [0x36314134, 1, K, N, g]
+    assert np.all(buf[20:256] == 0)
+    assert np.array_equal(q[:K, :N], oracle.awq_unpack(L.qweight, N))
+    assert np.all(q[K:] == 0) and np.all(q[:, N:] == 0)
+    G = K // g
+    assert np.array_equal(s[:G, :N], L.scales_bits)
+    assert np.array_equal(z[:G, :N], oracle.awq_unpack(L.qzeros, N))
+    assert np.all(s[G:] == 0) and np.all(s[:, N:] == 0) and np.all(z[G:] == 0) and np.all(z[:, N:] == 0)
+
+
+# ------------------------------------------------------------------ chunked repack: byte-identical
+
+def _repack_chunked(L, chunk, compact):
+    K, N, g = L.K, L.N, L.g
+    out = torch.full_like(L.packed, 0xAB)
+    for n0 in range(0, N, chunk):
+        n1 = min(n0 + chunk, N)
+        qw, qz, sc = L.d_qweight[:, n0 // 8:n1 // 8], L.d_qzeros[:, n0 // 8:n1 // 8], L.d_scales[:, n0:n1]
+        if compact:
+            qw, qz, sc = qw.contiguous(), qz.contiguous(), sc.contiguous()
+        w4.repack_chunk(qw, qz, sc, K, N, g, n0, n1, out)
+    return out
+
+
+@pytest.mark.parametrize("N,K", [(13312, 2048), (2048, 6656), (3072, 2048), (131072, 2048)])
+def test_chunked_repack_is_byte_identical(N, K):
+    L = Layer(K, N, 128, seed=4)
+    for chunk in (512, 4992):                  # 4992 columns: ragged last chunk
+        for compact in (False, True):
+            assert torch.equal(_repack_chunked(L, chunk, compact), L.packed), (chunk, compact)
+
+
+def test_chunked_repack_tail_block():
+    L = Layer(6656, 80, 32, seed=4)
+    assert torch.equal(_repack_chunked(L, 64, True), L.packed)
+
+
+# ------------------------------------------------------------------ GEMM parity
+
+GEMM_CASES = [
+    ("square", 1), ("qkv", 1), ("gate_up", 1), ("down", 1),
+    ("qkv", 16), ("gate_up", 16), ("down", 16),
+    ("qkv", 3), ("gate_up", 8), ("down", 12),
+    ("qkv", 512), ("gate_up", 512), ("down", 512),
+    ("square", 17), ("square", 129),
+]
+
+
+@pytest.mark.parametrize("name,M", GEMM_CASES)
+def test_gemm_layer_shapes(name, M):
+    K, N = SHAPES[name]
+    L = Layer(K, N, 128, seed=0)
+    x = inputs.make_x(M, K, seed=0)
+    _, y16 = L.ref(x)
+    assert_close(L.gemm(x), y16)
+
+
+@pytest.mark.parametrize("M", [1, 8, 512])
+def test_gemm_lm_head_sampled(M):
+    K, N = SHAPES["lm_head"]
+    L = Layer(K, N, 128, seed=0)
+    x = inputs.make_x(M, K, seed=1)
+    y = L.gemm(x).float().cpu().numpy()
+    rng = np.random.default_rng(M)
+    mi = rng.integers(0, M, 4096)
+    ni = np.concatenate([rng.integers(0, N, 4064), np.arange(N - 32, N)])
+    ref = oracle.linear_sampled(x.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, 128, mi, ni)
+    ref16 = oracle.double_to_half_bits(ref).view(np.float16).astype(np.float64)
+    mx, mean = errors(y[mi, ni], ref16)
+    assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("M", [1, 3, 17, 129])
+@pytest.mark.parametrize("zeros", ["sym8", "uniform"])
+def test_gemm_edge_tail(g, M, zeros):
+    K, N = SHAPES["tail80"]
+    L = Layer(K, N, g, seed=M, zeros=zeros, scale_dist="loguniform", scale_lo=1e-4, scale_hi=0.1)
+    x = inputs.make_x(M, K, seed=M)
+    _, y16 = L.ref(x)
+    assert_close(L.gemm(x), y16)
+
+
+@pytest.mark.parametrize("K,N,g,M", [(96, 8, 32, 5), (192, 72, 64, 2), (128, 64, 128, 1),
+                                     (224, 200, 32, 33), (4096, 264, 64, 16)])
+def test_gemm_small_ragged(K, N, g, M):
+    L = Layer(K, N, g, seed=7)
+    x = inputs.make_x(M, K, seed=7)
+    _, y16 = L.ref(x)
+    assert_close(L.gemm(x), y16)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 17, 130])
+@pytest.mark.parametrize("g", [32, 128])
+def test_gemm_bit_exact_when_sums_are_exact(M, g):
+    """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so the result must
+    equal the oracle bit for bit, whatever the summation order."""
+    K, N = 2048, 192
+    L = Layer(K, N, g, seed=8)
+    L.scales_bits = np.full_like(L.scales_bits, 0x1C00)          # 2^-8
+    L.d_scales = torch.from_numpy(L.scales_bits.view(np.float16)).to(dev())
+    L.packed = w4.repack(L.d_qweight, L.d_qzeros, L.d_scales, K, N, g)
+    xi = np.random.default_rng(M).integers(-2, 3, size=(M, K)).astype(np.float16)
+    _, y16 = L.ref(xi)
+    y = L.gemm(xi).cpu().numpy().view(np.uint16)
+    assert np.array_equal(y, y16)
+
+
+def test_gemm_q_equal_z_gives_zero():
+    K, N, g = 1024, 256, 64
+    L = Layer(K, N, g, seed=9)
+    L.qweight = np.repeat(L.qzeros, g, axis=0)
+    L.d_qweight = torch.from_numpy(L.qweight).to(dev())
+    L.packed = w4.repack(L.d_qweight, L.d_qzeros, L.d_scales, K, N, g)
+    for M in (1, 16, 64):
+        y = L.gemm(inputs.make_x(M, K, seed=M))
+        assert torch.all(y == 0)
+
+
+@pytest.mark.parametrize("M", [1, 16, 512])
+def test_gemm_deterministic(M):
+    K, N = SHAPES["gate_up"]
+    L = Layer(K, N, 128, seed=10)
+    x = inputs.make_x(M, K, seed=10)
+    a, b = L.gemm(x), L.gemm(x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N", [(3, 80), (17, 80), (129, 136), (1, 2048)])
+def test_gemm_guard_bands(M, N):
+    K, g = 512, 64
+    L = Layer(K, N, g, seed=11)
+    buf = torch.full((M * N + 8192,), 1234.0, dtype=torch.float16, device=dev())
+    y = buf[4096:4096 + M * N].view(M, N)
+    x = inputs.make_x(M, K, seed=11)
+    L.gemm(x, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:4096] == 1234.0) and torch.all(buf[4096 + M * N:] == 1234.0)
+    _, y16 = L.ref(x)
+    assert_close(y, y16)
+
+
+def test_gemm_m0_is_noop():
+    L = Layer(256, 64, 128, seed=12)
+    y = torch.full((1, 64), 5.0, dtype=torch.float16, device=dev())
+    x = torch.zeros((1, 256), dtype=torch.float16, device=dev())
+    w4.gemm(x, L.packed, 0, 64, 256, 128, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(y == 5.0)
+
+
+def test_header_mismatch_is_reported_and_nothing_written():
+    K, N, g = 512, 128, 128
+    L = Layer(K, N, g, seed=13)
+    assert w4.last_device_error() == 0
+    bad = L.packed.clone()
+    bad[0] ^= 0xFF                                       # corrupt the magic
+    x = torch.from_numpy(inputs.make_x(2, K)).to(dev())
+    y = torch.full((2, N), 7.0, dtype=torch.float16, device=dev())
+    w4.gemm(x, bad, 2, N, K, g, y=y)
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    assert torch.all(y == 7.0)
+    W = torch.full((K, N), 7.0, dtype=torch.float16, device=dev())
+    w4.dequant(bad, K, N, g, out=W)
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    assert torch.all(W == 7.0)
+    # a smaller N than the buffer was packed for is also caught (and reads stay in bounds)
+    w4.gemm(x, L.packed, 2, 64, K, g, y=y[:, :64].contiguous())
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    # the record is cleared and a correct call runs clean
+    y_ok = w4.gemm(x, L.packed, 2, N, K, g)
+    assert w4.last_device_error() == 0
+    _, y16 = L.ref(x.cpu().numpy())
+    assert_close(y_ok, y16)
+
+
+def test_nondefault_stream():
+    K, N, g = 2048, 3072, 128
+    L = Layer(K, N, g, seed=14)
+    x = inputs.make_x(4, K, seed=14)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        xd = torch.from_numpy(x).to(dev())
+        y = w4.gemm(xd, L.packed, 4, N, K, g)
+    s.synchronize()
+    _, y16 = L.ref(x)
+    assert_close(y, y16)

@@ -1,0 +1,9 @@
+"""GB300 (sm_103a) asymmetric group-wise W4A16 linear layer.
+
+    y = x . W,   W[k, n] = (q[k, n] - z[k // g, n]) * s[k // g, n]
+
+The compute is a C-ABI CUDA library (include/w4a16.h, csrc/); ``binding`` marshals torch
+tensors into it.  ``inputs`` draws the seeded synthetic tensors used by tests and benchmarks.
+"""
+from .binding import (W4A16Error, dequant, gemm, last_device_error, layout_version,  # noqa: F401
+                      packed_bytes, repack, repack_chunk, status_string, workspace_bytes)

@@ -1,0 +1,153 @@
+"""ctypes binding of the C ABI in include/w4a16.h (argument marshalling only).
+
+Every step of the layer runs in the library's CUDA kernels; this module only turns torch
+tensors into device pointers and the current CUDA stream into a stream handle, allocates
+outputs when the caller does not pass them, and raises on a non-zero status.  There is no CPU
+fallback: if the shared library is missing or fails to load, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_libw4a16.so")
+
+OK = 0
+ERR_INVALID = -1
+ERR_UNSUPPORTED = -2
+ERR_MISALIGNED = -3
+ERR_WORKSPACE = -4
+ERR_CUDA = -5
+ERR_DEVICE = -6
+
+# name -> (argtypes, restype) of every extern "C" entry point of include/w4a16.h
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "w4a16_packed_bytes": ([_I, _I, _I], _SZ),
+    "w4a16_workspace_bytes": ([_I, _I, _I, _I], _SZ),
+    "w4a16_repack": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "w4a16_repack_chunk": ([_P, _I64, _P, _I64, _P, _I64, _I, _I, _I, _I, _I, _P, _P], _I),
+    "w4a16_gemm": ([_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "w4a16_dequant": ([_P, _I, _I, _I, _P, _P], _I),
+    "w4a16_status_string": ([_I], ctypes.c_char_p),
+    "w4a16_last_device_error": ([_P], _I),
+    "w4a16_layout_version": ([], _I),
+}
+
+_lib = None
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %d (%s)" % (fn, status, status_string(status)))
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("CUDA library %s is missing: run __graft_entry__.build() first" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    return lib().w4a16_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != OK:
+        raise W4A16Error(fn, status)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def layout_version():
+    return lib().w4a16_layout_version()
+
+
+def packed_bytes(K, N, g):
+    return lib().w4a16_packed_bytes(K, N, g)
+
+
+def workspace_bytes(M, N, K, g):
+    return lib().w4a16_workspace_bytes(M, N, K, g)
+
+
+def repack(qweight, qzeros, scales, K, N, g, packed=None, stream=None):
+    """AWQ qweight int32 [K, N/8], qzeros int32 [K/g, N/8], scales fp16 [K/g, N] -> packed uint8."""
+    _dev(qweight, torch.int32, "qweight")
+    _dev(qzeros, torch.int32, "qzeros")
+    _dev(scales, torch.float16, "scales")
+    nbytes = packed_bytes(K, N, g)
+    if nbytes == 0:
+        _check("w4a16_packed_bytes", ERR_UNSUPPORTED)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    _check("w4a16_repack", lib().w4a16_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, g,
+                                              _ptr(packed), _stream(stream)))
+    return packed
+
+
+def repack_chunk(qweight_c, qzeros_c, scales_c, K, N, g, n0, n1, packed, stream=None):
+    """Repack columns [n0, n1) given the column slices (2-D tensors, unit inner stride)."""
+    for t, name in ((qweight_c, "qweight"), (qzeros_c, "qzeros"), (scales_c, "scales")):
+        if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s slice must be a 2-D CUDA tensor with unit column stride" % name)
+    _check("w4a16_repack_chunk", lib().w4a16_repack_chunk(
+        _ptr(qweight_c), qweight_c.stride(0), _ptr(qzeros_c), qzeros_c.stride(0),
+        _ptr(scales_c), scales_c.stride(0), K, N, g, n0, n1, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
+    """y fp16 [M, N] = x fp16 [M, K] . W(packed)."""
+    _dev(x, torch.float16, "x")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    need = workspace_bytes(M, N, K, g)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("w4a16_gemm", lib().w4a16_gemm(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y), ws_ptr, ws_len,
+                                          _stream(stream)))
+    return y
+
+
+def dequant(packed, K, N, g, out=None, stream=None):
+    """fp16 W [K, N] from the packed buffer (bit-exact)."""
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float16, device=packed.device)
+    _check("w4a16_dequant", lib().w4a16_dequant(_ptr(packed), K, N, g, _ptr(out), _stream(stream)))
+    return out
+
+
+def last_device_error(stream=None):
+    """Synchronize the stream and return (and clear) the device-side error status."""
+    return lib().w4a16_last_device_error(_stream(stream))

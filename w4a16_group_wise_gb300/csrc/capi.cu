@@ -1,0 +1,156 @@
+// capi.cu -- the extern "C" entry points of include/w4a16.h: argument validation (the analogue
+// of vLLM's verify_marlin_supported, "Carga de capas cuantizadas", section "Limites y
+// fallos"), the choice between the decode and the tensor-core path by M (vllm-omni commit
+// "Add cpu_int4 ...": two paths over one set of weights), and the per-device error word.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "kernels.h"
+#include "layout.cuh"
+
+using namespace w4a16;
+
+// Per-device error word: kernels record device-side failures here (never trap).
+static __device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int *g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+int *device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int K, int N, int g) {
+  if (K <= 0 || N <= 0 || g <= 0) return W4A16_ERR_INVALID;
+  if (g != 32 && g != 64 && g != 128) return W4A16_ERR_UNSUPPORTED;
+  if (N % 8 != 0 || K % g != 0) return W4A16_ERR_UNSUPPORTED;
+  return W4A16_OK;
+}
+
+int map_launch(cudaError_t e) {
+  if (e == cudaSuccess) return W4A16_OK;
+  cudaGetLastError();  // clear a sticky-free launch error so the next call starts clean
+  return W4A16_ERR_CUDA;
+}
+
+}  // namespace
+
+// Only the entry points of include/w4a16.h are exported; everything else is hidden.
+#pragma GCC visibility push(default)
+extern "C" {
+
+size_t w4a16_packed_bytes(int K, int N, int g) {
+  if (check_shape(K, N, g) != W4A16_OK) return 0;
+  return (size_t)kHeaderBytes + (size_t)num_nblocks(N) * num_ktiles(K) * chunk_bytes(g);
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
+  (void)M; (void)N; (void)K; (void)g;
+  return 0;
+}
+
+int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c,
+                       int64_t ld_qzeros, const uint16_t *scales_c, int64_t ld_scales, int K, int N,
+                       int g, int n0, int n1, void *packed, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!qweight_c || !qzeros_c || !scales_c || !packed) return W4A16_ERR_INVALID;
+  if (n0 < 0 || n1 > N || n0 >= n1 || n0 % kBlockN != 0 || (n1 % kBlockN != 0 && n1 != N))
+    return W4A16_ERR_INVALID;
+  int64_t w = (n1 - n0) / 8;
+  if (ld_qweight < w || ld_qzeros < w || ld_scales < (int64_t)(n1 - n0)) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(qweight_c) & 3u) ||
+      (reinterpret_cast<uintptr_t>(qzeros_c) & 3u) || (reinterpret_cast<uintptr_t>(scales_c) & 1u))
+    return W4A16_ERR_MISALIGNED;
+  return map_launch(launch_repack(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales,
+                                  K, N, g, n0, n1, packed, static_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_repack(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K,
+                 int N, int g, void *packed, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!qweight || !qzeros || !scales || !packed) return W4A16_ERR_INVALID;
+  if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(packed))
+    return W4A16_ERR_MISALIGNED;
+  return w4a16_repack_chunk(qweight, N / 8, qzeros, N / 8, scales, N, K, N, g, 0, N, packed,
+                            stream);
+}
+
+int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+               void *workspace, size_t workspace_bytes, void *stream) {
+  if (M < 0) return W4A16_ERR_INVALID;
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!x || !packed || !y) return W4A16_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+  size_t need = w4a16_workspace_bytes(M, N, K, g);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return map_launch(launch_gemv(x, packed, M, N, K, g, y, err, s));
+}
+
+int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!packed || !W) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || !aligned16(W)) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_dequant(packed, K, N, g, W, err, static_cast<cudaStream_t>(stream)));
+}
+
+const char *w4a16_status_string(int status) {
+  switch (status) {
+    case W4A16_OK: return "ok";
+    case W4A16_ERR_INVALID: return "invalid argument (null pointer, non-positive size or bad n-range)";
+    case W4A16_ERR_UNSUPPORTED: return "unsupported shape (need N % 8 == 0, K % g == 0, g in {32, 64, 128})";
+    case W4A16_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case W4A16_ERR_WORKSPACE: return "workspace smaller than w4a16_workspace_bytes";
+    case W4A16_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case W4A16_ERR_DEVICE: return "device-side error (packed header mismatch or wait timeout)";
+    default: return "unknown status";
+  }
+}
+
+int w4a16_last_device_error(void *stream) {
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (v != 0) {
+    int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    return W4A16_ERR_DEVICE;
+  }
+  return W4A16_OK;
+}
+
+int w4a16_layout_version(void) { return (int)kLayoutVersion; }
+
+}  // extern "C"
+#pragma GCC visibility pop

@@ -1,0 +1,25 @@
+// kernels.h -- host-side launchers of the library's CUDA kernels (internal; the public ABI is
+// include/w4a16.h).  Every launcher has been handed validated arguments and returns the
+// cudaError_t of its launch.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4a16 {
+
+// Repack columns [n0, n1) of AWQ tensors (slices starting at column n0, row strides in
+// elements) into their n-blocks of `packed`, and write the header.
+cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
+                          const uint16_t *scales, int64_t lds, int K, int N, int g, int n0, int n1,
+                          void *packed, cudaStream_t stream);
+
+// packed -> fp16 W[K][N].
+cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W, int *err,
+                           cudaStream_t stream);
+
+// Decode path: y = x . W for 1 <= M (rows are processed 16 at a time).
+cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g,
+                        uint16_t *y, int *err, cudaStream_t stream);
+
+}  // namespace w4a16
