@@ -398,6 +398,29 @@ def workload_config(n_launches=3 * LAYERS, packed_mb=None, world=1):
     return cfg
 
 
+def run_profile_case(spec):
+    """A small fixed case for ncu: 2 warm-up launches, then 3 launches (capture with -s 2 -c 3)."""
+    import torch
+    import __graft_entry__
+    import w4a16_group_wise_gb300 as w4
+
+    __graft_entry__.build()
+    name, M = spec.split(":")
+    M = int(M)
+    K, N = inputs.SHAPES[name]
+    dev = torch.device("cuda", 0)
+    h = inputs.make_weights(K, N, G, seed=0)
+    packed = w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                       torch.from_numpy(h["scales"]).to(dev), K, N, G)
+    x = torch.from_numpy(inputs.make_x(M, K, seed=0)).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    for _ in range(5):
+        w4.gemm(x, packed, M, N, K, G, y=y)
+    torch.cuda.synchronize()
+    assert w4.last_device_error() == 0
+    print("profile case %s M=%d done" % (name, M))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,6 +428,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", metavar="SHAPE:M", default=None,
+                    help="no timing: repack one layer of SHAPE (qkv, gate_up, down, lm_head, ...) and run "
+                         "a few gemm launches with M rows, for a profiler to capture")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
 
@@ -419,6 +445,9 @@ def main():
         return
 
     import torch
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")

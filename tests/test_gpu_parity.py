@@ -285,3 +285,19 @@ def test_nondefault_stream():
     s.synchronize()
     _, y16 = L.ref(x)
     assert_close(y, y16)
+
+
+@pytest.mark.parametrize("K,N,g,M", [(4096, 19456, 128, 1), (4096, 19456, 64, 16), (8192, 20480, 32, 3)])
+def test_gemm_long_k_ring_refill(K, N, g, M):
+    """Enough n-blocks that K is not split and more chunks per CTA than shared-memory ring slots,
+    so ring slots are refilled; checked on sampled outputs."""
+    L = Layer(K, N, g, seed=15)
+    x = inputs.make_x(M, K, seed=15)
+    y = L.gemm(x).float().cpu().numpy()
+    rng = np.random.default_rng(15)
+    mi = rng.integers(0, M, 3000)
+    ni = np.concatenate([rng.integers(0, N, 2936), np.arange(64), np.arange(N - 64, N)])[:3000]
+    ref = oracle.linear_sampled(x.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, g, mi, ni)
+    ref16 = oracle.double_to_half_bits(ref).view(np.float16).astype(np.float64)
+    mx, mean = errors(y[mi, ni], ref16)
+    assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);
     bad = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g);
-    if (bad) atomicExch(err, 1);
+    if (bad) atomicOr(err, 1);
   }
 
   for (int u = threadIdx.x; u < kBlockN * 4; u += blockDim.x) {

@@ -1,50 +1,48 @@
-// gemv.cu -- decode path of y = x . W for few rows of x (M <= 16 per m-block).
+// gemv.cu -- decode path of y = x . W for few rows of x (up to 16 per m-block).
 //
 // Why a separate path: "single-stream decode reads every weight to emit one token, so bits
 // per weight set the token rate" (vllm-omni commit "Add cpu_int4, an asymmetric 4-bit weight
-// path for vLLM's CPU backend").  The kernel streams the packed weights exactly once with
-// 128-bit coalesced loads, converts nibbles to fp16 in registers (dq.cuh), and lets the tensor
-// pipe do the multiply-adds (mma.sync m16n8k16, fp16 x fp16 -> fp32) so that the conversion
-// work, not the FMAs, is what the CUDA cores issue.  The weight tile is the A operand
-// (16 columns n x 16 k) and x^T the B operand (16 k x 8 rows m), so M <= 8 costs one MMA per
-// 256 weights and M <= 16 two.
+// path for vLLM's CPU backend").  The kernel streams the packed weights exactly once, with
+// enough bytes in flight for HBM and as little fixed latency per launch as possible:
+//  - one CTA owns RT row-tiles (16 columns each) of one 64-column n-block over the whole of K,
+//    so there is no reduction across CTAs; its W warps take the 128-k chunks round-robin;
+//  - every lane loads its codes with 16-byte non-allocating loads (a warp's load covers 8
+//    column-rows x 128 k = 512 contiguous bytes), software-pipelined about 4 KB deep per warp;
+//    the weights are requested before waiting on the previous kernel in the stream
+//    (programmatic dependent launch: they are read-only);
+//  - x (L1-cached loads, zero past M and K) is fetched one chunk ahead of its use (staging it
+//    in shared memory first was measured slower: every warp then waits for all of x);
+//  - nibbles are converted to fp16 in registers (dq.cuh) and the tensor pipe does the
+//    multiply-adds (mma.sync m16n8k16, fp16 x fp16 -> fp32), so the CUDA cores only issue the
+//    conversion.  The weight tile is the A operand (16 columns n x 16 k) and x^T the B operand
+//    (16 k x 8 rows m): M <= 8 costs one MMA per 256 weights, M <= 16 two.
+// (Bulk asynchronous copies of the weights into shared memory were measured slower here: the
+// copies of one CTA complete about one at a time, so a CTA's stream is latency-bound unless
+// each copy is tens of KB.)
 //
-// k permutation: inside a 128-k chunk, lane (r8 = lane/4, t = lane%4) owns the 32-k span
-// [32t, 32t+32) of its column-rows.  MMA step j (0..7) maps the fragment's logical k
-// {2t, 2t+1, 2t+8, 2t+9} to physical k 32t + 4j + {0, 1, 2, 3}; A and B fragments use the same
-// map (both index k by t), so the products are unchanged and every lane reads contiguous data.
+// k permutation inside a 128-k chunk: lane (r8 = lane/4, t = lane%4) owns the 32-k span
+// [32t, 32t+32) of its column-rows; MMA step j maps the fragment's logical k {2t, 2t+1, 2t+8,
+// 2t+9} to physical k 32t + 4j + {0, 1, 2, 3}.  A and B fragments both index k by t, so the
+// products are unchanged and every lane reads contiguous data.
 //
-// Scale: for g = 128 a chunk is one group, so the MMA chain over the chunk's 8 steps sums
-// (q - z) * x exactly in fp32 and the fp32 scale is applied once per (column, row of x)
-// afterwards.  For g = 32 / 64 the chain spans several groups and each weight is multiplied by
-// its scale in fp16 (the exact fp16 weight) before the MMA.
+// Scale: for g = 128 a chunk is one group, so each chunk's MMA chains sum (q - z) * x exactly in
+// fp32 and the fp32 scale is applied once per (column, row of x) at the end of the chunk.  For
+// g = 32 / 64 a chain spans several groups and each weight is multiplied by its scale in fp16
+// (the exact fp16 weight) before the MMA.
 //
-// Split of K: the W warps of a CTA take the CTA's chunks round-robin; the S CTAs of a thread
-// block cluster (S <= 8) take consecutive K ranges of the same n-block.  Partial sums are added
-// in a fixed order (warps 0..W-1, then cluster ranks 0..S-1 read through distributed shared
-// memory), so y is bit-identical from run to run and no global workspace is needed.
-#include <cooperative_groups.h>
+// The warps' partial sums are added in warp order through shared memory, so y is bit-identical
+// from run to run.
 #include <cuda_runtime.h>
 
 #include "dq.cuh"
 #include "kernels.h"
 #include "layout.cuh"
-
-namespace cg = cooperative_groups;
+#include "ptx.cuh"
 
 namespace w4a16 {
 namespace {
 
-constexpr int kMaxWarps = 4;
-constexpr int kMaxCluster = 8;
-
-__device__ __forceinline__ uint4 ld_stream(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kMaxWarps = 16;
 
 __device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -55,209 +53,419 @@ __device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// MB: 8-row blocks of x handled per CTA (1: M <= 8, 2: M <= 16).  FACTOR: scale applied per
-// chunk in fp32 (g == 128) instead of per weight in fp16.
-template <int MB, bool FACTOR>
-__global__ void __launch_bounds__(kMaxWarps * 32) gemv_kernel(
-    const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g,
-    int KT, int chunks_per_cta, uint16_t *__restrict__ y, int *err) {
-  constexpr int kVals = 16 * MB;  // accumulator values per lane: 4 row-tiles x MB x 4
-  __shared__ float red[kMaxWarps][kVals][32];
-  __shared__ float part[kVals * 32];
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream4(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream1(const void *p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// What one lane holds for one chunk of weights.
+template <int RT>
+struct Stage {
+  uint4 code[RT][2];   // [row-tile][rows r8, r8 + 8], 32 k each
+  uint32_t scale[RT];  // fp16 scales of rows r8 (low half) and r8 + 8 (high half)
+  uint32_t zero[RT];   // zero codes: bits 0..3 row r8, bits 4..7 row r8 + 8
+};
+
+// x[m][32 k of the lane's span], m = m0 + r8 (+ 8); zeros past M or K
+template <int MB>
+struct XFrag {
+  uint4 v[MB][4];
+};
+
+// RT: row-tiles per CTA (1 or 2).  MB: 8-row blocks of x (1: M <= 8, 2: M <= 16).  FACTOR:
+// scale applied per chunk in fp32 (g == 128) instead of per weight in fp16.
+// Sixteen warps are only launched for RT == 1, MB == 1; the other variants get more registers.
+template <int RT, int MB>
+constexpr int kThreadBound = (RT == 1 && MB == 1) ? kMaxWarps * 32 : kMaxWarps * 16;
+
+template <int RT, int MB, bool FACTOR>
+__global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16_t *__restrict__ x,
+                                                              const uint8_t *__restrict__ packed, int M, int N,
+                                                              int K, int g, int KT, uint16_t *__restrict__ y,
+                                                              int *err) {
+  constexpr int kDepth = 4 / RT;      // chunks of weights in flight per warp (~4 KB); even
+  constexpr int kVals = RT * MB * 4;  // accumulator values per lane
+  extern __shared__ __align__(16) float red[];  // [W][kVals][32]
   __shared__ int bad;
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
   const int r8 = lane >> 2, t = lane & 3;
-  const int b = blockIdx.x;
-  const int S = gridDim.y, s = blockIdx.y;
-  const int m0 = blockIdx.z * 8 * MB;
+  const int tile0 = blockIdx.x * RT;  // first row-tile (16 columns) of this CTA
+  const int b = tile0 / 4, i0 = tile0 % 4;
+  const int m0 = blockIdx.y * 8 * MB;
   const int CB = chunk_bytes(g);
-  const int kt_begin = s * chunks_per_cta;
-  const int kt_end = min(KT, kt_begin + chunks_per_cta);
   const uint8_t *body = packed + kHeaderBytes + (size_t)b * KT * CB;
+  const int mine = (KT - warp + W - 1) / W;  // chunks warp, warp + W, ...
 
-  float acc[4][MB][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[i][mb][c] = 0.f;
+  int hdr_ok = 1;
+  if (threadIdx.x == 0) {
+    const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
+    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g);
+  }
 
-#pragma unroll 1
-  for (int kt = kt_begin + warp; kt < kt_end; kt += nwarps) {
-    const uint8_t *chunk = body + (size_t)kt * CB;
-    uint4 cw[4][2];
+  auto load_w = [&](Stage<RT> &st, int j) {
+    const uint8_t *ch = body + (size_t)(warp + j * W) * CB;
+    const uint8_t *meta = ch + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int r = 0; r < RT; ++r) {
+      const int i = i0 + r;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) cw[i][h] = ld_stream(chunk + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
-    const uint8_t *meta = chunk + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
-    const uint4 sc = __ldg(reinterpret_cast<const uint4 *>(meta) + r8);
-    const uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + r8);
-
-    const int kx = kt * kTileK + 32 * t;
-    uint4 xf[MB][4];
+      for (int h = 0; h < 2; ++h) st.code[r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
+      st.scale[r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
+      st.zero[r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+    }
+  };
+  auto load_x = [&](XFrag<MB> &xf, int j) {
+    const int kx = (warp + j * W) * kTileK + 32 * t;
 #pragma unroll
     for (int mb = 0; mb < MB; ++mb) {
       const int m = m0 + 8 * mb + r8;
-      const bool ok = (m < M) && (kx < K);
-      const uint4 *xp = reinterpret_cast<const uint4 *>(x + (size_t)(ok ? m : 0) * K + (ok ? kx : 0));
+      const bool in = (m < M) && (kx < K);
+      const uint4 *xp = reinterpret_cast<const uint4 *>(x + (size_t)(in ? m : 0) * K + (in ? kx : 0));
 #pragma unroll
-      for (int q = 0; q < 4; ++q) xf[mb][q] = ok ? __ldg(xp + q) : make_uint4(0, 0, 0, 0);
+      for (int q = 0; q < 4; ++q) xf.v[mb][q] = in ? __ldg(xp + q) : make_uint4(0, 0, 0, 0);
     }
-    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+  };
 
+  float acc[RT][MB][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // scales of rows 16i + r8 (h = 0) and 16i + r8 + 8 (h = 1): halves 2i and 2i+1 of sc
-      const uint32_t s_lo = scw[i] & 0xFFFFu, s_hi = scw[i] >> 16;
-      const ZeroBias zb0 = zero_bias((zw >> (8 * i)) & 0xFu);
-      const ZeroBias zb1 = zero_bias((zw >> (8 * i + 4)) & 0xFu);
-      float d[MB][4];
-#pragma unroll
-      for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) d[mb][c] = 0.f;
-      const uint32_t w0[4] = {cw[i][0].x, cw[i][0].y, cw[i][0].z, cw[i][0].w};
-      const uint32_t w1[4] = {cw[i][1].x, cw[i][1].y, cw[i][1].z, cw[i][1].w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t v0[4], v1[4];
-        word_to_qz(w0[w], zb0, v0);
-        word_to_qz(w1[w], zb1, v1);
-        if (!FACTOR) {
-          const uint32_t s20 = s_lo * 0x00010001u, s21 = s_hi * 0x00010001u;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v0[e] = hmul2_u32(v0[e], s20);
-            v1[e] = hmul2_u32(v1[e], s21);
-          }
-        }
-#pragma unroll
-        for (int mb = 0; mb < MB; ++mb) {
-          float *dst = FACTOR ? d[mb] : acc[i][mb];
-          const uint32_t xs[4] = {xf[mb][w].x, xf[mb][w].y, xf[mb][w].z, xf[mb][w].w};
-          mma16816(dst, v0[0], v1[0], v0[1], v1[1], xs[0], xs[1]);  // k 8w + 0..3
-          mma16816(dst, v0[2], v1[2], v0[3], v1[3], xs[2], xs[3]);  // k 8w + 4..7
-        }
-      }
-      if (FACTOR) {
-        const float f0 = __half2float(__ushort_as_half((unsigned short)s_lo));
-        const float f1 = __half2float(__ushort_as_half((unsigned short)s_hi));
-#pragma unroll
-        for (int mb = 0; mb < MB; ++mb) {
-          acc[i][mb][0] = fmaf(f0, d[mb][0], acc[i][mb][0]);
-          acc[i][mb][1] = fmaf(f0, d[mb][1], acc[i][mb][1]);
-          acc[i][mb][2] = fmaf(f1, d[mb][2], acc[i][mb][2]);
-          acc[i][mb][3] = fmaf(f1, d[mb][3], acc[i][mb][3]);
-        }
-      }
-    }
-  }
-
-  // ---- deterministic reduction: warps in order, then cluster ranks in order
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int r = 0; r < RT; ++r)
 #pragma unroll
     for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) red[warp][(i * MB + mb) * 4 + c][lane] = acc[i][mb][c];
-  if (threadIdx.x == 0) {
-    const Header *h = reinterpret_cast<const Header *>(packed);
-    bad = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g);
-    if (bad && b == 0 && s == 0 && blockIdx.z == 0) atomicExch(err, 1);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < kVals * 32; e += blockDim.x) {
-    float v = 0.f;
-    for (int w = 0; w < nwarps; ++w) v += red[w][e / 32][e % 32];
-    part[e] = v;
-  }
+      for (int c = 0; c < 4; ++c) acc[r][mb][c] = 0.f;
 
-  bool write = true;
-  if (S > 1) {
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    write = cluster.block_rank() == 0;
-    if (write) {
-      for (int e = threadIdx.x; e < kVals * 32; e += blockDim.x) {
-        float v = 0.f;
-        for (int rk = 0; rk < S; ++rk) v += cluster.map_shared_rank(part, rk)[e];
-        part[e] = v;  // only rank 0 rewrites its own entry after every rank has been read
+  Stage<RT> st[kDepth];
+  XFrag<MB> xa, xb;  // x of the current and the next chunk, alternating
+#pragma unroll
+  for (int d = 0; d < kDepth; ++d)
+    if (d < mine) load_w(st[d], d);
+  griddep_launch_dependents();
+  griddep_wait();  // x may be the previous kernel's output; y may still be read by it
+  if (mine > 0) load_x(xa, 0);
+
+#pragma unroll 1
+  for (int j0 = 0; j0 < mine; j0 += kDepth) {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+      const int j = j0 + d;
+      if (j < mine) {
+        XFrag<MB> &xc = (d & 1) ? xb : xa;
+        XFrag<MB> &xn = (d & 1) ? xa : xb;
+        if (j + 1 < mine) load_x(xn, j + 1);
+        Stage<RT> &s = st[d];
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          const ZeroBias zb0 = zero_bias(s.zero[r] & 0xFu), zb1 = zero_bias((s.zero[r] >> 4) & 0xFu);
+          float dd[MB][4];
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dd[mb][e] = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t w0 = (w == 0) ? s.code[r][0].x : (w == 1) ? s.code[r][0].y : (w == 2) ? s.code[r][0].z : s.code[r][0].w;
+            const uint32_t w1 = (w == 0) ? s.code[r][1].x : (w == 1) ? s.code[r][1].y : (w == 2) ? s.code[r][1].z : s.code[r][1].w;
+            uint32_t v0[4], v1[4];
+            word_to_qz(w0, zb0, v0);
+            word_to_qz(w1, zb1, v1);
+            if (!FACTOR) {
+              const uint32_t s20 = (s.scale[r] & 0xFFFFu) * 0x00010001u, s21 = (s.scale[r] >> 16) * 0x00010001u;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v0[e] = hmul2_u32(v0[e], s20);
+                v1[e] = hmul2_u32(v1[e], s21);
+              }
+            }
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+              float *dst = FACTOR ? dd[mb] : acc[r][mb];
+              const uint4 xw = xc.v[mb][w];
+              mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+              mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+            }
+          }
+          if (FACTOR) {
+            const float f0 = __half2float(__ushort_as_half((unsigned short)(s.scale[r] & 0xFFFFu)));
+            const float f1 = __half2float(__ushort_as_half((unsigned short)(s.scale[r] >> 16)));
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+              acc[r][mb][0] = fmaf(f0, dd[mb][0], acc[r][mb][0]);
+              acc[r][mb][1] = fmaf(f0, dd[mb][1], acc[r][mb][1]);
+              acc[r][mb][2] = fmaf(f1, dd[mb][2], acc[r][mb][2]);
+              acc[r][mb][3] = fmaf(f1, dd[mb][3], acc[r][mb][3]);
+            }
+          }
+        }
+        if (j + kDepth < mine) load_w(s, j + kDepth);
       }
     }
-    cluster.sync();
-  } else {
-    __syncthreads();
   }
-  if (!write || bad) return;
-  if (S > 1) __syncthreads();
 
+  // ---------------------------------------------------------------- reduction over warps
+#pragma unroll
+  for (int r = 0; r < RT; ++r)
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) red[(warp * kVals + (r * MB + mb) * 4 + c) * 32 + lane] = acc[r][mb][c];
+  if (threadIdx.x == 0) bad = !hdr_ok;
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) atomicOr(err, 1);
+    return;
+  }
   for (int e = threadIdx.x; e < kVals * 32; e += blockDim.x) {
     const int ln = e % 32, vi = e / 32;
-    const int c = vi % 4, mb = (vi / 4) % MB, i = vi / (4 * MB);
-    const int row = 16 * i + (ln >> 2) + 8 * (c >> 1);
+    float v = 0.f;
+    for (int w = 0; w < W; ++w) v += red[(w * kVals + vi) * 32 + ln];
+    const int c = vi % 4, mb = (vi / 4) % MB, r = vi / (4 * MB);
+    const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = m0 + 8 * mb + 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
-    if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(part[e]));
+    if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(v));
   }
 }
 
-template <int MB, bool FACTOR>
-cudaError_t launch_variant(dim3 grid, int warps, int S, const uint16_t *x, const uint8_t *packed, int M,
-                           int N, int K, int g, int KT, int cpc, uint16_t *y, int *err,
-                           cudaStream_t stream) {
+
+// ---------------------------------------------------------------------------------------------
+// Lean variant for M <= 4 (the decode case): a warp streams its x slices into a private
+// shared-memory ring with cp.async, issued together with the weights D chunks ahead, so x costs
+// no registers and the kernel fits in <= 64 registers per thread -- four 8-warp CTAs per SM.
+// HBM throughput of plain loads follows the number of warps with loads outstanding more than
+// the bytes each has in flight, so this is what lets the decode stream reach the bandwidth.
+constexpr int kSmallRows = 4;   // rows of x per CTA in the lean variant
+constexpr int kSmallWarps = 8;
+
+template <int D, bool FACTOR>
+__global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
+    const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
+    uint16_t *__restrict__ y, int *err) {
+  // x ring: [warp][D slots][kSmallRows rows][128 k] fp16 = 1 KB per slot
+  __shared__ __align__(16) uint8_t xring[kSmallWarps][D][kSmallRows * 256];
+  __shared__ float red[kSmallWarps][4][32];
+  __shared__ int bad;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r8 = lane >> 2, t = lane & 3;
+  const int tile = blockIdx.x;
+  const int b = tile / 4, i = tile % 4;
+  const int CB = chunk_bytes(g);
+  const uint8_t *body = packed + kHeaderBytes + (size_t)b * KT * CB;
+  const int mine = (KT - warp + kSmallWarps - 1) / kSmallWarps;  // chunks warp, warp + 8, ...
+
+  int hdr_ok = 1;
+  if (threadIdx.x == 0) {
+    const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
+    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g);
+  }
+
+  uint4 code[D][2];
+  uint32_t scale[D], zero[D];
+  auto load_w = [&](int d, int j) {
+    const uint8_t *ch = body + (size_t)(warp + j * kSmallWarps) * CB;
+    const uint8_t *meta = ch + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) code[d][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
+    scale[d] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
+    zero[d] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+  };
+  // x rows 0..M-1 of chunk j into slot d: M * 16 pieces of 16 bytes, lane p takes pieces p, p+32..
+  auto load_x = [&](int d, int j) {
+    const int k0 = (warp + j * kSmallWarps) * kTileK;
+    for (int p = lane; p < M * 16; p += 32) {
+      const int m = p / 16, q = p % 16;
+      const bool ok = k0 + 8 * q < K;
+      cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
+    }
+  };
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int d = 0; d < D; ++d)
+    if (d < mine) load_w(d, d);
+  griddep_launch_dependents();
+  griddep_wait();  // x may be the previous kernel's output; y may still be read by it
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    if (d < mine) load_x(d, d);
+    cp_async_commit();  // one group per slot, possibly empty
+  }
+
+#pragma unroll 1
+  for (int j0 = 0; j0 < mine; j0 += D) {
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int j = j0 + d;
+      if (j < mine) {
+        cp_async_wait_pending<D - 1>();  // this slot's x has landed (for this lane's pieces)
+        __syncwarp();                     // ... and every lane's pieces are visible
+        const ZeroBias zb0 = zero_bias(zero[d] & 0xFu), zb1 = zero_bias((zero[d] >> 4) & 0xFu);
+        const uint8_t *xs = &xring[warp][d][r8 * 256 + 64 * t];
+        const bool xrow = r8 < M;
+        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t w0 = (w == 0) ? code[d][0].x : (w == 1) ? code[d][0].y : (w == 2) ? code[d][0].z : code[d][0].w;
+          const uint32_t w1 = (w == 0) ? code[d][1].x : (w == 1) ? code[d][1].y : (w == 2) ? code[d][1].z : code[d][1].w;
+          uint32_t v0[4], v1[4];
+          word_to_qz(w0, zb0, v0);
+          word_to_qz(w1, zb1, v1);
+          if (!FACTOR) {
+            const uint32_t s20 = (scale[d] & 0xFFFFu) * 0x00010001u, s21 = (scale[d] >> 16) * 0x00010001u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v0[e] = hmul2_u32(v0[e], s20);
+              v1[e] = hmul2_u32(v1[e], s21);
+            }
+          }
+          const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
+          float *dst = FACTOR ? dd : acc;
+          mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+          mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+        }
+        if (FACTOR) {
+          const float f0 = __half2float(__ushort_as_half((unsigned short)(scale[d] & 0xFFFFu)));
+          const float f1 = __half2float(__ushort_as_half((unsigned short)(scale[d] >> 16)));
+          acc[0] = fmaf(f0, dd[0], acc[0]);
+          acc[1] = fmaf(f0, dd[1], acc[1]);
+          acc[2] = fmaf(f1, dd[2], acc[2]);
+          acc[3] = fmaf(f1, dd[3], acc[3]);
+        }
+        __syncwarp();  // every lane is done reading the slot before it is refilled
+        if (j + D < mine) {
+          load_w(d, j + D);
+          load_x(d, j + D);
+        }
+        cp_async_commit();
+      }
+    }
+  }
+
+#pragma unroll
+  for (int c = 0; c < 4; ++c) red[warp][c][lane] = acc[c];
+  if (threadIdx.x == 0) bad = !hdr_ok;
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) atomicOr(err, 1);
+    return;
+  }
+  if (threadIdx.x < 128) {
+    const int ln = threadIdx.x % 32, c = threadIdx.x / 32;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSmallWarps; ++w) v += red[w][c][ln];
+    const int row = 16 * i + (ln >> 2) + 8 * (c >> 1);
+    const int m = 2 * (ln & 3) + (c & 1);
+    const int n = b * kBlockN + row;
+    if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(v));
+  }
+}
+
+
+int sm_count() {
+  static int count[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!count[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    count[dev] = c > 0 ? c : 148;
+  }
+  return count[dev];
+}
+
+template <int RT, int MB, bool FACTOR>
+cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, const uint8_t *packed, int M, int N,
+                           int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
+  const int smem = W * RT * MB * 4 * 32 * 4;
+  static bool configured[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<RT, MB, FACTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         160 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(32 * warps);
+  cfg.gridDim = dim3((tiles + RT - 1) / RT, mblocks);
+  cfg.blockDim = dim3(32 * W);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<RT, MB, FACTOR>, x, packed, M, N, K, g, KT, y, err);
+}
+
+template <int RT>
+cudaError_t launch_rt(int tiles, int mblocks, int W, int MB, bool factor, const uint16_t *x, const uint8_t *p,
+                      int M, int N, int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
+  if (MB == 1)
+    return factor ? launch_variant<RT, 1, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
+                  : launch_variant<RT, 1, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
+  return factor ? launch_variant<RT, 2, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
+                : launch_variant<RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
+}
+
+template <int D>
+cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
+                         int KT, uint16_t *y, int *err, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles);
+  cfg.blockDim = dim3(32 * kSmallWarps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  int na = 0;
-  if (S > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 1;
-    attr[na].val.clusterDim.y = S;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<MB, FACTOR>, x, packed, M, N, K, g, KT, cpc, y, err);
-}
-
-int sm_count() {
-  static int count = 0;
-  if (!count) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
-    if (count <= 0) count = 148;
-  }
-  return count;
+  cfg.numAttrs = 1;
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, true>, x, p, M, N, K, g, KT, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, false>, x, p, M, N, K, g, KT, y, err);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                         int *err, cudaStream_t stream) {
-  const int NB = num_nblocks(N), KT = num_ktiles(K);
+  const int KT = num_ktiles(K);
   const int MB = (M <= 8) ? 1 : 2;
   const int mblocks = (M + 8 * MB - 1) / (8 * MB);
-  // Split K over a cluster until the grid covers the GPU about twice.
-  int S = 1;
-  while (S < kMaxCluster && S * 2 <= KT && (long)NB * S * mblocks < 2L * sm_count()) S *= 2;
-  const int cpc = (KT + S - 1) / S;  // chunks per CTA
-  const int warps = cpc < kMaxWarps ? cpc : kMaxWarps;
-  dim3 grid(NB, S, mblocks);
+  // Row-tiles of 16 columns that hold at least one column < N (N % 8 == 0).
+  const int tiles = (N + 15) / 16;
   const uint8_t *p = static_cast<const uint8_t *>(packed);
   const bool factor = (g == kTileK);
-  if (MB == 1)
-    return factor ? launch_variant<1, true>(grid, warps, S, x, p, M, N, K, g, KT, cpc, y, err, stream)
-                  : launch_variant<1, false>(grid, warps, S, x, p, M, N, K, g, KT, cpc, y, err, stream);
-  return factor ? launch_variant<2, true>(grid, warps, S, x, p, M, N, K, g, KT, cpc, y, err, stream)
-                : launch_variant<2, false>(grid, warps, S, x, p, M, N, K, g, KT, cpc, y, err, stream);
+  const long ctas1 = (long)tiles * mblocks;
+  // Lean variant for M <= 4 unless K is long and the grid is small (then 16 warps per CTA win).
+  const bool long_k = KT >= 32 && ctas1 <= sm_count();
+  if (M <= kSmallRows && !long_k) return launch_small<2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+  // Two row-tiles per CTA once the grid would cover the GPU several times over (a 2-tile CTA
+  // never straddles an n-block: tiles come in fours per n-block and pairs start at even tiles);
+  // with 16 rows of x the per-CTA weights are reused twice as often, so earlier.  Four warps on
+  // large grids, sixteen when K is long and the grid is at most about one CTA per SM (measured).
+  const int sms = sm_count();
+  const bool two = ctas1 >= (MB == 1 ? 4L : 1L) * sms;
+  const int W = (ctas1 >= 4L * sms) ? 4 : (!two && long_k && MB == 1) ? 16 : 8;
+  if (two) return launch_rt<2>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+  return launch_rt<1>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
 }
 
 }  // namespace w4a16
