@@ -106,7 +106,8 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return map_launch(launch_gemv(x, packed, M, N, K, g, y, err, s));
+  if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, g, y, err, s));
+  return map_launch(launch_gemm_tc(x, packed, M, N, K, g, y, err, s));
 }
 
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {

@@ -22,4 +22,14 @@ cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W,
 cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g,
                         uint16_t *y, int *err, cudaStream_t stream);
 
+// Tensor-core path (tcgen05): y = x . W for M > 16.
+cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+                           int *err, cudaStream_t stream);
+
+// Rows of x per CTA tile of the tensor-core path.
+int gemm_tc_block_m(int M);
+
+// Largest M the decode path takes.
+constexpr int kDecodeMaxM = 16;
+
 }  // namespace w4a16
