@@ -282,15 +282,16 @@ def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, pea
     for si, (name, K, N) in enumerate(DECODE_SHAPES):
         x = torch.from_numpy(inputs.make_x(M, K, seed=77)).to(dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        ws = torch.zeros(max(1, w4.workspace_bytes(M, N, K, G)), dtype=torch.uint8, device=dev)
         sel = [lin[si][3] for lin in layers]
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             for p in sel:
-                w4.gemm(x, p, M, N, K, G, y=y, stream=stream)
+                w4.gemm(x, p, M, N, K, G, y=y, workspace=ws, stream=stream)
         stream.synchronize()
         with torch.cuda.graph(g2, stream=stream):
             for p in sel:
-                w4.gemm(x, p, M, N, K, G, y=y, stream=stream)
+                w4.gemm(x, p, M, N, K, G, y=y, workspace=ws, stream=stream)
         for _ in range(3):
             g2.replay()
         reps = min(200, max(5, args.steps // 4))

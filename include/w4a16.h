@@ -84,8 +84,14 @@ extern "C" {
  * or unsupported. */
 size_t w4a16_packed_bytes(int K, int N, int g);
 
-/* Bytes of device workspace w4a16_gemm needs for this problem; 0 means none (workspace may
- * then be NULL).  Stable for given arguments. */
+/* Bytes of device workspace w4a16_gemm needs for this problem on the current device; 0 means
+ * none (workspace may then be NULL).  The tensor-core path splits K across CTAs when the output
+ * tiles alone would leave SMs idle; the workspace then holds 4096 bytes of per-tile arrival
+ * counters at offset 0 followed by fp32 partial tiles.  Stable for given arguments on a given
+ * device.  The first 4096 bytes must be zero before the first use; every call that completes
+ * leaves them zero (whatever its shape), so one buffer, sized for the largest problem, serves
+ * call after call.  Calls that share a workspace must not overlap on the GPU (one workspace per
+ * concurrent stream).  After a device-side error, zero the first 4096 bytes again. */
 size_t w4a16_workspace_bytes(int M, int N, int K, int g);
 
 /* One-time repack of AWQ tensors into the packed layout (integer-exact; scales copied bit for
@@ -109,9 +115,13 @@ int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight,
 /* y = x . W.  x fp16 bits [M][K] row-major, y fp16 bits [M][N] row-major (fully written),
  * packed from w4a16_repack with the same K, N, g.  M == 0 is a no-op.  M <= 16 takes the
  * decode path (fused dequant + skinny GEMM streaming the packed weights once); larger M the
- * tensor-core path.  Accumulation is in fp32; the result is rounded once to fp16 and is
- * bit-identical from run to run.  workspace: w4a16_workspace_bytes(M, N, K, g) bytes of device
- * memory (may be NULL when that is 0). */
+ * tensor-core path (weights dequantized to fp16 tile by tile in shared memory, tcgen05 MMAs
+ * with fp32 accumulation in tensor memory).  Accumulation is in fp32; the result is rounded
+ * once to fp16 and is bit-identical from run to run.  workspace: w4a16_workspace_bytes(M, N,
+ * K, g) bytes of 16-byte aligned device memory (may be NULL when that is 0), see there.
+ * A w4a16_gemm may start reading `packed` while the previous w4a16_gemm on the same stream is
+ * still running (programmatic dependent launch); it reads x and writes y only after that one
+ * has completed. */
 int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                void *workspace, size_t workspace_bytes, void *stream);
 

@@ -301,3 +301,37 @@ def test_gemm_long_k_ring_refill(K, N, g, M):
     ref16 = oracle.double_to_half_bits(ref).view(np.float16).astype(np.float64)
     mx, mean = errors(y[mi, ni], ref16)
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
+
+
+@pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 129), ("square", 40)])
+def test_gemm_split_k_workspace_reuse(name, M):
+    """Where the tensor-core path splits K, one zero-filled workspace serves call after call:
+    every completed call leaves its arrival counters at zero, and results are bit-identical."""
+    K, N = SHAPES[name]
+    L = Layer(K, N, 128, seed=16)
+    need = w4.workspace_bytes(M, N, K, 128)
+    assert need > 0, "expected a split-K plan for this shape"
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device=dev())   # partials need no init
+    ws[:4096] = 0
+    x = inputs.make_x(M, K, seed=16)
+    ys = [L.gemm(x, workspace=ws) for _ in range(3)]
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+    torch.cuda.synchronize()
+    # the arrival counters (first 4096 bytes) are all back to zero
+    assert int(torch.count_nonzero(ws[:4096])) == 0
+    _, y16 = L.ref(x)
+    assert_close(ys[0], y16)
+
+
+def test_gemm_workspace_too_small_is_rejected():
+    K, N = SHAPES["down"]
+    L = Layer(K, N, 128, seed=17)
+    M = 512
+    need = w4.workspace_bytes(M, N, K, 128)
+    assert need > 0
+    small = torch.zeros(need - 16, dtype=torch.uint8, device=dev())
+    x = torch.from_numpy(inputs.make_x(M, K)).to(dev())
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.gemm(x, L.packed, M, N, K, 128, workspace=small)
+    assert e.value.status == w4.binding.ERR_WORKSPACE

@@ -125,6 +125,21 @@ def repack_chunk(qweight_c, qzeros_c, scales_c, K, N, g, n0, n1, packed, stream=
     return packed
 
 
+_workspaces = {}
+
+
+def default_workspace(nbytes, device):
+    """A zero-filled workspace of at least `nbytes` bytes, cached per device.  Every completed
+    call leaves it zero-filled, so it is reused; calls on different streams that may overlap
+    need workspaces of their own."""
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
     """y fp16 [M, N] = x fp16 [M, K] . W(packed)."""
     _dev(x, torch.float16, "x")
@@ -132,7 +147,7 @@ def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     need = workspace_bytes(M, N, K, g)
     if need and workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+        workspace = default_workspace(need, x.device)
     ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("w4a16_gemm", lib().w4a16_gemm(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y), ws_ptr, ws_len,

@@ -61,8 +61,9 @@ size_t w4a16_packed_bytes(int K, int N, int g) {
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
-  (void)M; (void)N; (void)K; (void)g;
-  return 0;
+  if (M < 0 || check_shape(K, N, g) != W4A16_OK) return 0;
+  if (M <= kDecodeMaxM) return 0;
+  return gemm_tc_workspace_bytes(M, N, K);
 }
 
 int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c,
@@ -103,11 +104,12 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
   if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
   size_t need = w4a16_workspace_bytes(M, N, K, g);
   if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, g, y, err, s));
-  return map_launch(launch_gemm_tc(x, packed, M, N, K, g, y, err, s));
+  return map_launch(launch_gemm_tc(x, packed, M, N, K, g, y, err, workspace, s));
 }
 
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {

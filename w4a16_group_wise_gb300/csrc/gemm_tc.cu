@@ -36,12 +36,12 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kBN = 128;          // weight rows (output columns n) per CTA = MMA M
-constexpr int kBK = 128;          // k per stage (one packed chunk)
-constexpr int kAtomK = 64;        // k per 128-byte swizzle atom (fp16)
-constexpr int kAStageBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kMaxStages = 4;
-constexpr int kThreads = 256;
+constexpr int kBN = 128;                      // weight rows (output columns n) per CTA = MMA M
+constexpr int kBK = 64;                       // k per stage: one 128-byte swizzle atom of fp16
+constexpr int kAStageBytes = kBN * kBK * 2;   // 16 KB
+constexpr int kMaxStages = 6;
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4..11 dequant; all: epilogue
+constexpr int kDeqThreads = 256;
 
 struct GemmSmem {
   int stages, bm;
@@ -112,27 +112,41 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 // --------------------------------------------------------------------------- the kernel
 
+// Split-K plan: each (n-tile, m-tile) is cut into `splits` consecutive ranges of 64-k stages.
+// With splits > 1 every CTA stores its fp32 partial tile into the workspace and the last one
+// to finish a tile (per-tile arrival counter) adds the partials in split order and writes y.
+struct SplitPlan {
+  int splits;
+  int stages_per_split;  // 64-k stages per split (the last split may have fewer)
+  float *partials;       // [splits][tiles][bm][128] fp32
+  int *counters;         // [tiles], zero between calls
+};
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const uint8_t *__restrict__ packed, int M, int N,
                                                                int K, int g, int KT, int bm, int stages,
-                                                               int tmem_cols, uint16_t *__restrict__ y, int *err) {
+                                                               int tmem_cols, SplitPlan sp, uint16_t *__restrict__ y,
+                                                               int *err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle pattern repeats every 1024 bytes)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ int flags;
+  __shared__ int flags, last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmSmem L = gemm_smem(bm, stages);
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bm;
   const int NB = num_nblocks(N);
   const int CB = chunk_bytes(g);
+  const int KS = (K + kBK - 1) / kBK;  // 64-k stages over K (a padded half chunk is skipped)
+  const int st_begin = blockIdx.z * sp.stages_per_split;
+  const int nst = max(0, min(KS, st_begin + sp.stages_per_split) - st_begin);
   const uint32_t x_bytes = (uint32_t)bm * kBK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full_bar[s], 1 + 128);  // TMA expect-tx arrival + 128 dequant threads
+      mbar_init(&full_bar[s], 1 + kDeqThreads);  // TMA expect-tx arrival + dequant threads
       mbar_init(&empty_bar[s], 1);       // one tcgen05.commit per use
     }
     mbar_init(&accum_bar, 1);
@@ -158,20 +172,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       griddep_wait();  // x may be the previous kernel's output
       bool ok = true;
       int issued = 0;
-      for (int kb = 0; kb < KT; ++kb) {
-        const int s = kb % stages, use = kb / stages;
-        if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
-        uint8_t *b = smem + s * L.stage_bytes + L.b_off;
+      for (int j = 0; j < nst; ++j) {
+        const int s = j % stages, use = j / stages;
+        if (use > 0 && !(ok = mbar_wait_sleep_bounded(&empty_bar[s], (use - 1) & 1))) break;
         mbar_arrive_expect_tx(&full_bar[s], x_bytes);
-        tma_load_2d(b, &xmap, kb * kBK, m0, &full_bar[s]);
-        tma_load_2d(b + bm * 128, &xmap, kb * kBK + kAtomK, m0, &full_bar[s]);
+        tma_load_2d(smem + s * L.stage_bytes + L.b_off, &xmap, (st_begin + j) * kBK, m0, &full_bar[s]);
         ++issued;
       }
       if (!ok) {
         atomicOr(&flags, 2);
         // let every issued copy land before the CTA may exit
-        for (int kb = (issued > stages ? issued - stages : 0); kb < issued; ++kb)
-          mbar_wait_bounded(&full_bar[kb % stages], (kb / stages) & 1);
+        for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
+          mbar_wait_bounded(&full_bar[j % stages], (j / stages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -179,110 +191,176 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(bm);
       bool ok = true;
-      for (int kb = 0; kb < KT; ++kb) {
-        const int s = kb % stages, use = kb / stages;
-        if (!(ok = mbar_wait_bounded(&full_bar[s], use & 1))) break;
+      for (int j = 0; j < nst; ++j) {
+        const int s = j % stages, use = j / stages;
+        if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
         tc_fence_after();
         const uint8_t *a = smem + s * L.stage_bytes + L.a_off;
         const uint8_t *b = smem + s * L.stage_bytes + L.b_off;
 #pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          const int atom = ks / 4, kin = (ks % 4) * 32;  // bytes within the 128-byte row
-          const uint64_t ad = sw128_desc(a + atom * (kBN * 128) + kin);
-          const uint64_t bd = sw128_desc(b + atom * (bm * 128) + kin);
-          mma_f16(tmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kBK / 16; ++ks)  // 32 bytes of each 128-byte row per MMA
+          mma_f16(tmem, sw128_desc(a + 32 * ks), sw128_desc(b + 32 * ks), idesc, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
       }
       if (!ok) atomicOr(&flags, 2);
       mma_commit(&accum_bar);  // the accumulator is final once every MMA above completes
+      if (!mbar_wait_sleep_bounded(&accum_bar, 0)) atomicOr(&flags, 2);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dequant producers
-    const int t = threadIdx.x - 128;            // column-row of the tile, 0..127
-    const int b = (n0 >> 6) + (t >> 6);         // n-block of this row
-    const int r = t & 63;                        // row inside the n-block
-    const bool have = b < NB;                    // the last tile may have one n-block only
+    // thread t: column-row r of the tile, 32-k quarter-row hw of each 64-k stage
+    const int t = threadIdx.x - 128;
+    const int r = t & (kBN - 1), hw = t >> 7;
+    const int b = (n0 >> 6) + (r >> 6);          // n-block of this row
+    const int rr = r & 63;                        // row inside the n-block
+    const bool have = b < NB;                     // the last tile may hold one n-block only
     const uint8_t *body = packed + kHeaderBytes + (size_t)(have ? b : 0) * KT * CB;
-    const int gpc = kTileK / g;
-    const int p = meta_pos(r);
+    const int p = meta_pos(rr);
     bool ok = true;
-    // codes and meta of the next k-block are fetched one k-block ahead
-    uint4 cw[4];
-    uint32_t sc[4], zw[4];
-    auto fetch = [&](int kb) {
-      const uint8_t *ch = body + (size_t)kb * CB;
+    // 32 k of codes (16 bytes) and their group's scale and zero, kPf stages ahead: the packed
+    // weights come from HBM and a stage's MMAs take well under the load latency
+    constexpr int kPf = 4;
+    uint4 pc[kPf];
+    uint32_t ps[kPf], pz[kPf];
+    auto fetch = [&](int d, int gs) {  // global 64-k stage gs: chunk gs / 2, half gs % 2
+      const uint8_t *ch = body + (size_t)(gs >> 1) * CB;
+      const int k32 = 2 * (gs & 1) + hw;  // 32-k span of the chunk
+      const uint8_t *meta = ch + kCodeBytes + ((32 * k32) / g) * kGroupMetaBytes;
+      pc[d] = have ? __ldg(reinterpret_cast<const uint4 *>(ch + rr * kRowBytes) + k32) : make_uint4(0, 0, 0, 0);
+      ps[d] = have ? __ldg(reinterpret_cast<const uint16_t *>(meta) + p) : 0u;
+      pz[d] = have ? __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8) : 0u;
+    };
 #pragma unroll
-      for (int q = 0; q < 4; ++q) cw[q] = have ? __ldg(reinterpret_cast<const uint4 *>(ch + r * kRowBytes) + q)
-                                            : make_uint4(0, 0, 0, 0);
+    for (int d = 0; d < kPf; ++d)
+      if (d < nst) fetch(d, st_begin + d);
+    for (int j0 = 0; j0 < nst && ok; j0 += kPf) {
 #pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        if (l < gpc && have) {
-          const uint8_t *meta = ch + kCodeBytes + l * kGroupMetaBytes;
-          sc[l] = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
-          zw[l] = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
-        } else {
-          sc[l] = 0;
-          zw[l] = 0;
+      for (int d = 0; d < kPf; ++d) {
+        const int j = j0 + d;
+        if (j < nst && ok) {
+          const int s = j % stages, use = j / stages;
+          if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
+          uint8_t *a = smem + s * L.stage_bytes + L.a_off;
+          const uint4 c = pc[d];
+          const ZeroBias zb = zero_bias((pz[d] >> (4 * (p % 8))) & 0xFu);
+          const uint32_t s2 = ps[d] * 0x00010001u;
+          if (j + kPf < nst) fetch(d, st_begin + j + kPf);
+          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t v[4];
+            word_to_qz(words[w], zb, v);
+            uint4 o;
+            o.x = hmul2_u32(v[0], s2);
+            o.y = hmul2_u32(v[1], s2);
+            o.z = hmul2_u32(v[2], s2);
+            o.w = hmul2_u32(v[3], s2);
+            const int cc = 4 * hw + w;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4 *>(a + r * 128 + ((cc ^ (r & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
+          mbar_arrive(&full_bar[s]);
         }
       }
-    };
-    fetch(0);
-    for (int kb = 0; kb < KT; ++kb) {
-      const int s = kb % stages, use = kb / stages;
-      uint4 c[4] = {cw[0], cw[1], cw[2], cw[3]};
-      uint32_t scl[4] = {sc[0], sc[1], sc[2], sc[3]}, zl[4] = {zw[0], zw[1], zw[2], zw[3]};
-      if (kb + 1 < KT) fetch(kb + 1);
-      if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
-      uint8_t *a = smem + s * L.stage_bytes + L.a_off;
-      const uint32_t words[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
-                                  c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
-#pragma unroll
-      for (int w = 0; w < 16; ++w) {
-        const int l = (8 * w) / g;  // group of these 8 k inside the chunk
-        const ZeroBias zb = zero_bias((zl[l] >> (4 * (p % 8))) & 0xFu);
-        const uint32_t s2 = scl[l] * 0x00010001u;
-        uint32_t v[4];
-        word_to_qz(words[w], zb, v);
-        uint4 o;
-        o.x = hmul2_u32(v[0], s2);
-        o.y = hmul2_u32(v[1], s2);
-        o.z = hmul2_u32(v[2], s2);
-        o.w = hmul2_u32(v[3], s2);
-        const int atom = w / 8, cc = w % 8;
-        *reinterpret_cast<uint4 *>(a + atom * (kBN * 128) + t * 128 + ((cc ^ (t & 7)) << 4)) = o;
-      }
-      fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
-      mbar_arrive(&full_bar[s]);
     }
     if (!ok) atomicOr(&flags, 2);
   }
 
-  // ------------------------------------------------------------ epilogue: TMEM -> y (all warps)
-  bool ok = mbar_wait_bounded(&accum_bar, 0);
+  // ------------------------------------------------------------ epilogue (all warps)
+  // Only the MMA lane waits for the accumulator (above); every other thread parks in the
+  // hardware barrier below instead of polling, so the producers keep the issue slots.
+  tc_fence_before();
+  __syncthreads();
   tc_fence_after();
-  if (!ok) atomicOr(&flags, 2);
   griddep_wait();  // every storing thread waits for the previous kernel (a no-op once satisfied)
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);
     if (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g) atomicOr(&flags, 1);
   }
   __syncthreads();
-  const int fl = flags;
-  if (!fl) {
-    const int quarter = warp & 3, half = warp >> 2;
-    const int n = n0 + 32 * quarter + lane;
-    for (int c0 = 16 * half; c0 < bm; c0 += 32) {
-      uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, v);
+  // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (column-rows n) and the 16-column groups c of the
+  // tile with c % 3 == w / 4; a per-warp 2 KB transpose buffer in the (now idle) stage memory
+  // turns each group into 16-byte stores of consecutive n.
+  const int quarter = warp & 3, third = warp >> 2;
+  const int nq = n0 + 32 * quarter;  // first column-row of this warp
+  uint8_t *tb = smem + warp * 2048;
+  const int tiles = gridDim.x * gridDim.y, tile = blockIdx.y * gridDim.x + blockIdx.x;
+  int fl = flags;
+  if (sp.splits > 1) {
+    // store this split's fp32 partial tile [bm][128], then count the arrival
+    float *mine = sp.partials + ((size_t)blockIdx.z * tiles + tile) * bm * kBN;
+    if (!fl) {
+      for (int c0 = 16 * third; c0 < bm; c0 += 48) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = m0 + c0 + j;
-        if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j])));
+        for (int j2 = 0; j2 < 16; ++j2) reinterpret_cast<uint32_t *>(tb)[j2 * 32 + lane] = v[j2];
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // 128 pieces of 4 floats: (m = piece / 8, n = 4 * (piece % 8))
+          const int pc = lane + 32 * q, j2 = pc >> 3, nn = 4 * (pc & 7);
+          __stcg(reinterpret_cast<float4 *>(mine + (size_t)(c0 + j2) * kBN + 32 * quarter + nn),
+                 *reinterpret_cast<const float4 *>(tb + (j2 * 32 + nn) * 4));
+        }
+        __syncwarp();
       }
     }
-  } else if (threadIdx.x == 0) {
-    atomicOr(err, fl);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicAdd(&sp.counters[tile], 1) == sp.splits - 1);
+    __syncthreads();
+    if (!last) {
+      fl = 0;  // errors are reported by the last CTA of the tile
+    } else {
+      __threadfence();
+      if (threadIdx.x == 0) sp.counters[tile] = 0;  // ready for the next call
+    }
+  }
+  if (sp.splits > 1 && !last) {
+    // nothing more to do
+  } else if (fl) {
+    if (threadIdx.x == 0) atomicOr(err, fl);
+  } else if (sp.splits > 1) {
+    // add the partials in split order, 4 consecutive n per piece
+    for (int c0 = 16 * third; c0 < bm; c0 += 48) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pc = lane + 32 * q, j2 = pc >> 3, nn = 4 * (pc & 7);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int z = 0; z < sp.splits; ++z) {
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+              sp.partials + (((size_t)z * tiles + tile) * bm + c0 + j2) * kBN + 32 * quarter + nn));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const int m = m0 + c0 + j2, n = nq + nn;
+        if (m < M && n < N) {
+          uint2 o;
+          o.x = h2_as_u32(__floats2half2_rn(acc.x, acc.y));
+          o.y = h2_as_u32(__floats2half2_rn(acc.z, acc.w));
+          *reinterpret_cast<uint2 *>(y + (size_t)m * N + n) = o;
+        }
+      }
+    }
+  } else {
+    for (int c0 = 16 * third; c0 < bm; c0 += 48) {
+      uint32_t v[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, v);
+      uint16_t *th = reinterpret_cast<uint16_t *>(tb);
+#pragma unroll
+      for (int j2 = 0; j2 < 16; ++j2) th[j2 * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j2])));
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
+        const int pc = lane + 32 * q, j2 = pc >> 2, nn = 8 * (pc & 3);
+        const int m = m0 + c0 + j2, n = nq + nn;
+        if (m < M && n < N)
+          *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
+      }
+      __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -307,30 +385,83 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+int sm_count_tc() {
+  static int count[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!count[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    count[dev] = c > 0 ? c : 148;
+  }
+  return count[dev];
+}
+
+// Workspace of a split-K launch: kCounterBytes of per-tile arrival counters at offset 0 (zero
+// before the first call, left zero by every completed call, whatever the shape), then the fp32
+// partial tiles (no initialisation needed).
+constexpr int kCounterBytes = 4096;
+constexpr int kMaxSplitTiles = kCounterBytes / 4;
+
+struct TcPlan {
+  int bm, stages, tmem_cols, splits, stages_per_split, tiles;
+  size_t partial_bytes;
+};
+
+TcPlan plan_tc(int M, int N, int K) {
+  TcPlan p;
+  p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
+  p.stages = 0;
+  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 200 * 1024) ++p.stages;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < p.bm) p.tmem_cols *= 2;
+  p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
+  const int KS = (K + kBK - 1) / kBK;
+  // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
+  // four 64-k stages per split.
+  const int sms = sm_count_tc();
+  p.splits = 1;
+  if (4 * p.tiles < 3 * sms && p.tiles <= kMaxSplitTiles) {
+    p.splits = sms / p.tiles;
+    if (p.splits > KS / 4) p.splits = KS / 4;
+    if (p.splits < 1) p.splits = 1;
+  }
+  p.stages_per_split = (KS + p.splits - 1) / p.splits;
+  p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
+  p.partial_bytes = p.splits > 1 ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
+  return p;
+}
+
 }  // namespace
 
-int gemm_tc_block_m(int M) { return M >= 256 ? 256 : ((M + 15) / 16) * 16; }
+size_t gemm_tc_workspace_bytes(int M, int N, int K) {
+  const TcPlan p = plan_tc(M, N, K);
+  return p.splits > 1 ? kCounterBytes + p.partial_bytes : 0;
+}
 
 cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y, int *err,
-                           cudaStream_t stream) {
-  const int bm = gemm_tc_block_m(M);
-  int stages = 0;
-  while (stages < kMaxStages && gemm_smem(bm, stages + 1).total <= 200 * 1024) ++stages;
-  const GemmSmem L = gemm_smem(bm, stages);
-  int tmem_cols = 32;
-  while (tmem_cols < bm) tmem_cols *= 2;
+                           void *workspace, cudaStream_t stream) {
+  const TcPlan P = plan_tc(M, N, K);
+  const GemmSmem L = gemm_smem(P.bm, P.stages);
 
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kAtomK, (cuuint32_t)bm};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)P.bm};
   const cuuint32_t es[2] = {1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+
+  SplitPlan sp;
+  sp.splits = P.splits;
+  sp.stages_per_split = P.stages_per_split;
+  sp.counters = P.splits > 1 ? static_cast<int *>(workspace) : nullptr;
+  sp.partials = P.splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
 
   static bool configured[64];
   int dev = 0;
@@ -341,7 +472,7 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((N + kBN - 1) / kBN, (M + bm - 1) / bm);
+  cfg.gridDim = dim3((N + kBN - 1) / kBN, (M + P.bm - 1) / P.bm, P.splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L.total + 1024;  // + alignment slack
   cfg.stream = stream;
@@ -351,7 +482,7 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, static_cast<const uint8_t *>(packed), M, N, K, g,
-                            num_ktiles(K), bm, stages, tmem_cols, y, err);
+                            num_ktiles(K), P.bm, P.stages, P.tmem_cols, sp, y, err);
 }
 
 }  // namespace w4a16

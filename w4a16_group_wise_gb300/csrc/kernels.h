@@ -22,12 +22,12 @@ cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W,
 cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g,
                         uint16_t *y, int *err, cudaStream_t stream);
 
-// Tensor-core path (tcgen05): y = x . W for M > 16.
+// Tensor-core path (tcgen05): y = x . W for M > 16.  `workspace` holds
+// gemm_tc_workspace_bytes(M, N, K) bytes (may be null when that is 0); its counters must be zero
+// before the first call and are left zero by every completed call.
 cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
-                           int *err, cudaStream_t stream);
-
-// Rows of x per CTA tile of the tensor-core path.
-int gemm_tc_block_m(int M);
+                           int *err, void *workspace, cudaStream_t stream);
+size_t gemm_tc_workspace_bytes(int M, int N, int K);
 
 // Largest M the decode path takes.
 constexpr int kDecodeMaxM = 16;

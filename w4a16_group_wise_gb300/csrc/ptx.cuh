@@ -48,6 +48,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep (up to `hint_ns`) until the phase completes instead
+// of returning at once: long waits then cost no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that sleeps between polls (for long waits by single threads).
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t parity,
+                                                        uint64_t limit_ns = 200000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it < (1u << 24); ++it) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns` nanoseconds (and in
 // any case after 2^30 polls).  Returns false on timeout; the caller records the error and
 // winds down instead of hanging the GPU.
