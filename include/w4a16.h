@@ -130,6 +130,25 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
  * dequantizer. */
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream);
 
+/* Size of the scratch array built into the library for w4a16_gemm_noalloc (24 MiB): every GPU
+ * that loads the library keeps this much device memory for the life of the process. */
+#define W4A16_NOALLOC_SCRATCH_BYTES (24u << 20)
+
+/* y = x . W like w4a16_gemm, for callers that cannot allocate device memory at all -- a runtime
+ * that plans every device buffer ahead and hands a layer only its inputs and outputs, a plugin
+ * host that forbids allocation after start-up, a latency-critical path where an allocation could
+ * stall or fail.  No workspace is passed: the split-K scratch of the tensor-core path lives in
+ * an array of W4A16_NOALLOC_SCRATCH_BYTES inside the library (no counterpart on the pages; this
+ * entry point exists only for such callers).  The caller still provides x, packed and y as for
+ * w4a16_gemm.  Returns W4A16_ERR_WORKSPACE when the problem's scratch (w4a16_workspace_bytes)
+ * exceeds that size.  All calls share the one array, so calls that overlap on the GPU race with
+ * each other and must be serialized.  The first call on a device sets that device up
+ * (looks up the array and clears the counters at its head, synchronously), so make it before
+ * capturing the stream; every completed call leaves those counters cleared again.  Never calls
+ * cudaMalloc, cudaFree or any other allocating routine. */
+int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+                       void *stream);
+
 /* Static description of a status code. */
 const char *w4a16_status_string(int status);
 

@@ -1,0 +1,56 @@
+"""w4a16_gemm_noalloc against w4a16_gemm, through the C ABI.
+
+w4a16_gemm_noalloc serves callers that cannot allocate device memory (a runtime that plans every
+buffer ahead, a host that forbids allocation after start-up, a latency-critical path): instead of
+a caller workspace it keeps the tensor-core path's split-K scratch in an array built into the
+library.  That array is shared by every call and keeps the previous call's contents, so the
+results are checked on two calls in a row, against the ordinary entry point, within the same
+tolerance as the other GEMM tests.  This file is collected last on purpose.
+"""
+import ctypes
+
+import pytest
+
+from gpu_util import MAX_TOL, MEAN_TOL, Layer, dev, errors, torch
+import w4a16_group_wise_gb300 as w4
+from w4a16_group_wise_gb300 import binding, inputs
+
+P = ctypes.c_void_p
+
+
+def _call(x, packed, M, N, K, g, y):
+    st = P(torch.cuda.current_stream().cuda_stream)
+    return binding.lib().w4a16_gemm_noalloc(P(x.data_ptr()), P(packed.data_ptr()), M, N, K, g, P(y.data_ptr()), st)
+
+
+# split-K shapes (scratch in use), a shape that needs none, the decode path, the N = 80 tail
+CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 512, 128), ("square", 40, 128),
+         ("gate_up", 512, 128), ("gate_up", 1, 128), ("tail80", 17, 32)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,M,g", CASES)
+def test_noalloc_matches_workspace_entry_point(name, M, g):
+    K, N = inputs.SHAPES[name]
+    L = Layer(K, N, g, seed=21)
+    x = torch.from_numpy(inputs.make_x(M, K, seed=21)).to(dev())
+    ref = w4.gemm(x, L.packed, M, N, K, g).float().cpu().numpy()
+    assert w4.workspace_bytes(M, N, K, g) <= 24 << 20  # within the built-in scratch
+    for _ in range(2):
+        y = torch.full((M, N), 3.0, dtype=torch.float16, device=dev())
+        assert _call(x, L.packed, M, N, K, g, y) == binding.OK
+        assert w4.last_device_error() == binding.OK
+        mx, mean = errors(y.float().cpu().numpy(), ref)
+        assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host():
+    import __graft_entry__
+    __graft_entry__.build()
+    L = binding.lib()
+    a, odd, nul = P(0x10000), P(0x10008), P(0)
+    assert L.w4a16_gemm_noalloc(a, a, 1, 2048, 2048, 100, a, nul) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_gemm_noalloc(a, a, -1, 2048, 2048, 128, a, nul) == binding.ERR_INVALID
+    assert L.w4a16_gemm_noalloc(nul, a, 1, 2048, 2048, 128, a, nul) == binding.ERR_INVALID
+    assert L.w4a16_gemm_noalloc(odd, a, 1, 2048, 2048, 128, a, nul) == binding.ERR_MISALIGNED
+    assert L.w4a16_gemm_noalloc(a, a, 0, 2048, 2048, 128, nul, nul) == binding.OK

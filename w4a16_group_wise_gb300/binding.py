@@ -33,6 +33,7 @@ SIGNATURES = {
     "w4a16_status_string": ([_I], ctypes.c_char_p),
     "w4a16_last_device_error": ([_P], _I),
     "w4a16_layout_version": ([], _I),
+    "w4a16_gemm_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
 }
 
 _lib = None
@@ -152,6 +153,16 @@ def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("w4a16_gemm", lib().w4a16_gemm(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y), ws_ptr, ws_len,
                                           _stream(stream)))
+    return y
+
+
+def gemm_noalloc(x, packed, M, N, K, g, y, stream=None):
+    """y = x . W without any workspace: for callers that cannot allocate device memory (the
+    library's built-in scratch array serves instead; overlapping calls race on it)."""
+    _dev(x, torch.float16, "x")
+    _dev(y, torch.float16, "y")
+    _check("w4a16_gemm_noalloc", lib().w4a16_gemm_noalloc(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y),
+                                                          _stream(stream)))
     return y
 
 

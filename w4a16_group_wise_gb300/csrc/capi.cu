@@ -17,12 +17,13 @@ using namespace w4a16;
 static __device__ int g_device_error;
 
 namespace {
-
 constexpr int kMaxDevices = 64;
 int *g_err_ptr[kMaxDevices];
 std::mutex g_err_mu;
+}  // namespace
 
-int *device_error_word() {
+// The per-device error word of the current device (resolved once per device).
+int *w4a16::device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_err_mu);
@@ -33,6 +34,8 @@ int *device_error_word() {
   }
   return g_err_ptr[dev];
 }
+
+namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -29,6 +29,9 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
                            int *err, void *workspace, cudaStream_t stream);
 size_t gemm_tc_workspace_bytes(int M, int N, int K);
 
+// Device address of the library's per-device error word on the current device (null on failure).
+int *device_error_word();
+
 // Largest M the decode path takes.
 constexpr int kDecodeMaxM = 16;
 
