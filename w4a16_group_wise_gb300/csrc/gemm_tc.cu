@@ -10,18 +10,25 @@
 //
 // Orientation: D[n][m] = sum_k W^T[n][k] * x^T[k][m], i.e. the MMA's M dimension (128) runs
 // over output columns n and its N dimension (BM <= 256) over rows m of x, so few rows of x
-// waste no tensor work.  Per k-block of 128 (one packed chunk):
-//  - one lane of warp 0 loads the x tile (BM rows x 128 k, fp16) with two TMA copies into a
-//    128-byte-swizzled K-major tile (rows past M and k past K read as 0);
-//  - warps 4..7 (one thread per column-row) load that row's 64 code bytes and its scales and
-//    zeros, convert them to the exact fp16 weights fp16((q - z) * s) (dq.cuh) and store them into
-//    the A tile with the same 128-byte swizzle, then fence the writes to the async proxy;
-//  - one lane of warp 1 issues 8 MMAs (K = 16 each) once both operands are in place and
-//    commits them to the stage's "empty" barrier, which frees the stage when they complete.
-// The stages form a ring; after the last k-block the accumulator is committed to a barrier,
-// and all 8 warps read it back (tcgen05.ld, 32 lanes x 16 columns each), round to fp16 and
-// store y.  Every wait is bounded: on a timeout the kernel records an error, drains, frees
-// tensor memory and skips the store.
+// waste no tensor work.  Roles:
+//  - one lane of warp 2 copies the packed chunks of the tile's two n-blocks (codes and their
+//    scales and zeros, contiguous in the packed layout) into a ring of shared-memory slots with
+//    bulk asynchronous copies, one 128-k chunk per slot;
+//  - one lane of warp 0 loads the x tile of each 64-k stage (BM rows x 64 k, fp16) with a TMA
+//    copy into a 128-byte-swizzled K-major tile (rows past M and k past K read as 0);
+//  - warps 4..11, in two groups taking alternate stages (one lane per column-row), read the
+//    codes from the slot, convert them to the exact fp16 weights fp16((q - z) * s) (dq.cuh) and
+//    store them into the stage's A tile with the same 128-byte swizzle, then fence the writes
+//    to the async proxy;
+//  - one lane of warp 1 issues 4 MMAs (K = 16 each) per stage once both operands are in place
+//    and commits them to the stage's "empty" barrier, which frees the stage when they complete.
+// Measured on GB300: one warp's stage (wait, read, convert, store, fence, arrive) is a chain of
+// about 1200 cycles, against about 700 cycles of MMAs per stage, so the warps must overlap
+// stages (two groups) and read ahead to keep the tensor cores fed.
+// After the last stage the accumulator is committed to a barrier, and all 12 warps read it
+// back (tcgen05.ld, 32 lanes x 16 columns each), round to fp16 and store y.  Every wait is
+// bounded: on a timeout the kernel records an error, drains, frees tensor memory and skips the
+// store.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -40,14 +47,18 @@ constexpr int kBN = 128;                      // weight rows (output columns n) 
 constexpr int kBK = 64;                       // k per stage: one 128-byte swizzle atom of fp16
 constexpr int kAStageBytes = kBN * kBK * 2;   // 16 KB
 constexpr int kMaxStages = 6;
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4..11 dequant; all: epilogue
+constexpr int kThreads = 384;   // warp 0 x TMA, warp 1 MMA, warp 2 code copies, warps 4..11 dequant
 constexpr int kDeqThreads = 256;
+constexpr int kDeqWarps = kDeqThreads / 32;
+constexpr int kCodeSlots = 3;         // 128-k chunks of codes in flight
+constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 160) at g = 32
 
 struct GemmSmem {
   int stages, bm;
-  int a_off, b_off, stage_bytes, total;
+  int a_off, b_off, stage_bytes, codes_off, total;
 };
 
+// [stages x (A tile, x tile)] [kCodeSlots x code slot]
 __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   GemmSmem s;
   s.bm = bm;
@@ -55,7 +66,8 @@ __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   s.stage_bytes = kAStageBytes + bm * kBK * 2;
   s.a_off = 0;
   s.b_off = kAStageBytes;
-  s.total = stages * s.stage_bytes;
+  s.codes_off = stages * s.stage_bytes;
+  s.total = s.codes_off + kCodeSlots * kCodeSlotBytes;
   return s;
 }
 
@@ -102,6 +114,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// global -> shared bulk copy (both 16-byte aligned, bytes a multiple of 16), completion as
+// transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -117,7 +138,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 // to finish a tile (per-tile arrival counter) adds the partials in split order and writes y.
 struct SplitPlan {
   int splits;
-  int stages_per_split;  // 64-k stages per split (the last split may have fewer)
+  int stages_per_split;  // 64-k stages per split, even (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
   int *counters;         // [tiles], zero between calls
 };
@@ -131,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   // 1024-byte alignment of the operand tiles (the swizzle pattern repeats every 1024 bytes)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
+  __shared__ uint64_t cfull_bar[kCodeSlots], cempty_bar[kCodeSlots];
   __shared__ uint32_t tmem_base;
   __shared__ int flags, last;
 
@@ -140,14 +162,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const int NB = num_nblocks(N);
   const int CB = chunk_bytes(g);
   const int KS = (K + kBK - 1) / kBK;  // 64-k stages over K (a padded half chunk is skipped)
-  const int st_begin = blockIdx.z * sp.stages_per_split;
+  const int st_begin = blockIdx.z * sp.stages_per_split;  // even: a split starts on a chunk
   const int nst = max(0, min(KS, st_begin + sp.stages_per_split) - st_begin);
+  const int nch = (nst + 1) / 2;  // 128-k chunks this CTA reads
   const uint32_t x_bytes = (uint32_t)bm * kBK * 2;
+  const int nb0 = n0 >> 6;                      // first n-block of the tile
+  const int nblk = (nb0 + 1 < NB) ? 2 : 1;      // the last tile may hold one n-block only
+  uint8_t *codes = smem + L.codes_off;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full_bar[s], 1 + kDeqThreads);  // TMA expect-tx arrival + dequant threads
-      mbar_init(&empty_bar[s], 1);       // one tcgen05.commit per use
+      mbar_init(&full_bar[s], 1 + kDeqWarps / 2);  // TMA expect-tx arrival + one per warp of a group
+      mbar_init(&empty_bar[s], 1);             // one tcgen05.commit per use
+    }
+    for (int c = 0; c < kCodeSlots; ++c) {
+      mbar_init(&cfull_bar[c], 1);             // expect-tx arrival of the bulk copies
+      mbar_init(&cempty_bar[c], kDeqWarps);    // every dequant warp is done reading the slot
     }
     mbar_init(&accum_bar, 1);
     flags = 0;
@@ -206,62 +236,107 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mma_commit(&accum_bar);  // the accumulator is final once every MMA above completes
       if (!mbar_wait_sleep_bounded(&accum_bar, 0)) atomicOr(&flags, 2);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ packed chunks by bulk copy
+    // (the packed weights are read-only: no need to wait for the previous kernel)
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int lc = 0; lc < nch; ++lc) {
+        const int cs = lc % kCodeSlots, use = lc / kCodeSlots;
+        if (use > 0 && !(ok = mbar_wait_sleep_bounded(&cempty_bar[cs], (use - 1) & 1))) break;
+        const int c = (st_begin >> 1) + lc;
+        mbar_arrive_expect_tx(&cfull_bar[cs], (uint32_t)(nblk * CB));
+        for (int q = 0; q < nblk; ++q)
+          bulk_load(codes + cs * kCodeSlotBytes + q * CB,
+                    packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + c) * CB, (uint32_t)CB, &cfull_bar[cs]);
+        ++issued;
+      }
+      if (!ok) atomicOr(&flags, 2);
+      // every issued copy has landed before the CTA may exit (at once in the normal case)
+      for (int lc = (issued > kCodeSlots ? issued - kCodeSlots : 0); lc < issued; ++lc)
+        mbar_wait_bounded(&cfull_bar[lc % kCodeSlots], (lc / kCodeSlots) & 1);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dequant producers
-    // thread t: column-row r of the tile, 32-k quarter-row hw of each 64-k stage
-    const int t = threadIdx.x - 128;
-    const int r = t & (kBN - 1), hw = t >> 7;
-    const int b = (n0 >> 6) + (r >> 6);          // n-block of this row
+    // Two groups of four warps take alternate 64-k stages (group gsel: stages gsel, gsel + 2,
+    // ...), so two stages are converted at once.  In a group, lane l of warp w converts
+    // column-row r = 32 (w % 4) + l: the 64 k of the stage are 32 code bytes of the row in the
+    // chunk slot (read one stage ahead, before the waits, to hide the shared-memory latency),
+    // giving eight 16-byte pieces of the swizzled A row.
+    const int gsel = (warp - 4) >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const bool have = nb0 + (r >> 6) < NB;        // the last tile may hold one n-block only
     const int rr = r & 63;                        // row inside the n-block
-    const bool have = b < NB;                     // the last tile may hold one n-block only
-    const uint8_t *body = packed + kHeaderBytes + (size_t)(have ? b : 0) * KT * CB;
     const int p = meta_pos(rr);
-    bool ok = true;
-    // 32 k of codes (16 bytes) and their group's scale and zero, kPf stages ahead: the packed
-    // weights come from HBM and a stage's MMAs take well under the load latency
-    constexpr int kPf = 4;
-    uint4 pc[kPf];
-    uint32_t ps[kPf], pz[kPf];
-    auto fetch = [&](int d, int gs) {  // global 64-k stage gs: chunk gs / 2, half gs % 2
-      const uint8_t *ch = body + (size_t)(gs >> 1) * CB;
-      const int k32 = 2 * (gs & 1) + hw;  // 32-k span of the chunk
-      const uint8_t *meta = ch + kCodeBytes + ((32 * k32) / g) * kGroupMetaBytes;
-      pc[d] = have ? __ldg(reinterpret_cast<const uint4 *>(ch + rr * kRowBytes) + k32) : make_uint4(0, 0, 0, 0);
-      ps[d] = have ? __ldg(reinterpret_cast<const uint16_t *>(meta) + p) : 0u;
-      pz[d] = have ? __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8) : 0u;
+    const int rot = (rr >> 1) & 1;                // read order of the two 16-byte halves (banks)
+    struct Codes {
+      uint4 h[2];                                 // k 0..31 and 32..63 of the stage
+      uint32_t sc[2], zw[2];                      // scale and zero word of each 32-k half
     };
+    auto read_codes = [&](int j, Codes &cd) {
+      const int cs = (j >> 1) % kCodeSlots;
+      const uint8_t *ch = codes + cs * kCodeSlotBytes + (r >> 6) * CB;  // this row's chunk copy
+      const int k64 = (st_begin + j) & 1;                              // stage half of the chunk
+      uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;                      // read 0: half rot, read 1: the other
+      uint32_t s0 = 0, s1 = 0, z0 = 0, z1 = 0;
+      if (have) {
+        const int ka = 2 * k64 + rot, kb = 2 * k64 + (rot ^ 1);
+        const uint8_t *ma = ch + kCodeBytes + ((32 * ka) / g) * kGroupMetaBytes;
+        const uint8_t *mb = ch + kCodeBytes + ((32 * kb) / g) * kGroupMetaBytes;
+        c0 = *reinterpret_cast<const uint4 *>(ch + rr * kRowBytes + 16 * ka);
+        c1 = *reinterpret_cast<const uint4 *>(ch + rr * kRowBytes + 16 * kb);
+        s0 = *reinterpret_cast<const uint16_t *>(ma + 2 * p);
+        s1 = *reinterpret_cast<const uint16_t *>(mb + 2 * p);
+        z0 = *reinterpret_cast<const uint32_t *>(ma + kScaleBytes + 4 * (p / 8));
+        z1 = *reinterpret_cast<const uint32_t *>(mb + kScaleBytes + 4 * (p / 8));
+      }
+      cd.h[0] = rot ? c1 : c0;
+      cd.h[1] = rot ? c0 : c1;
+      cd.sc[0] = rot ? s1 : s0;
+      cd.sc[1] = rot ? s0 : s1;
+      cd.zw[0] = rot ? z1 : z0;
+      cd.zw[1] = rot ? z0 : z1;
+    };
+    bool ok = true;
+    Codes cur;
+    if (gsel < nst) {
+      ok = mbar_wait_bounded(&cfull_bar[(gsel >> 1) % kCodeSlots], ((gsel >> 1) / kCodeSlots) & 1);
+      if (ok) read_codes(gsel, cur);
+    }
+    for (int j = gsel; j < nst && ok; j += 2) {
+      const int s = j % stages, use = j / stages;
+      // convert this stage's codes into registers
+      uint4 out[8];
 #pragma unroll
-    for (int d = 0; d < kPf; ++d)
-      if (d < nst) fetch(d, st_begin + d);
-    for (int j0 = 0; j0 < nst && ok; j0 += kPf) {
+      for (int hh = 0; hh < 2; ++hh) {
+        const ZeroBias zb = zero_bias((cur.zw[hh] >> (4 * (p % 8))) & 0xFu);
+        const uint32_t s2 = cur.sc[hh] * 0x00010001u;
+        const uint32_t words[4] = {cur.h[hh].x, cur.h[hh].y, cur.h[hh].z, cur.h[hh].w};
 #pragma unroll
-      for (int d = 0; d < kPf; ++d) {
-        const int j = j0 + d;
-        if (j < nst && ok) {
-          const int s = j % stages, use = j / stages;
-          if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
-          uint8_t *a = smem + s * L.stage_bytes + L.a_off;
-          const uint4 c = pc[d];
-          const ZeroBias zb = zero_bias((pz[d] >> (4 * (p % 8))) & 0xFu);
-          const uint32_t s2 = ps[d] * 0x00010001u;
-          if (j + kPf < nst) fetch(d, st_begin + j + kPf);
-          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t v[4];
-            word_to_qz(words[w], zb, v);
-            uint4 o;
-            o.x = hmul2_u32(v[0], s2);
-            o.y = hmul2_u32(v[1], s2);
-            o.z = hmul2_u32(v[2], s2);
-            o.w = hmul2_u32(v[3], s2);
-            const int cc = 4 * hw + w;  // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4 *>(a + r * 128 + ((cc ^ (r & 7)) << 4)) = o;
-          }
-          fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
-          mbar_arrive(&full_bar[s]);
+        for (int w = 0; w < 4; ++w) {
+          uint32_t v[4];
+          word_to_qz(words[w], zb, v);
+          out[4 * hh + w] = make_uint4(hmul2_u32(v[0], s2), hmul2_u32(v[1], s2), hmul2_u32(v[2], s2),
+                                       hmul2_u32(v[3], s2));
         }
       }
+      // every lane has its codes in registers: this group is done with the chunk's slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cempty_bar[(j >> 1) % kCodeSlots]);
+      // read the next stage of this group (the next chunk) while waiting for the stage buffer
+      const int jn = j + 2;
+      if (jn < nst) {
+        if (!(ok = mbar_wait_bounded(&cfull_bar[(jn >> 1) % kCodeSlots], ((jn >> 1) / kCodeSlots) & 1))) break;
+        read_codes(jn, cur);
+      }
+      if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
+      uint8_t *a = smem + s * L.stage_bytes + L.a_off + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4 *>(a + ((cc ^ (r & 7)) << 4)) = out[cc];
+      fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_bar[s]);
     }
     if (!ok) atomicOr(&flags, 2);
   }
@@ -413,7 +488,7 @@ TcPlan plan_tc(int M, int N, int K) {
   TcPlan p;
   p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
   p.stages = 0;
-  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 200 * 1024) ++p.stages;
+  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 220 * 1024) ++p.stages;
   p.tmem_cols = 32;
   while (p.tmem_cols < p.bm) p.tmem_cols *= 2;
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
@@ -428,6 +503,7 @@ TcPlan plan_tc(int M, int N, int K) {
     if (p.splits < 1) p.splits = 1;
   }
   p.stages_per_split = (KS + p.splits - 1) / p.splits;
+  p.stages_per_split += p.stages_per_split & 1;  // splits start on a 128-k chunk
   p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
   p.partial_bytes = p.splits > 1 ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
   return p;
@@ -467,7 +543,7 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 222 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
