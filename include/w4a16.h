@@ -84,14 +84,18 @@ extern "C" {
  * or unsupported. */
 size_t w4a16_packed_bytes(int K, int N, int g);
 
-/* Bytes of device workspace w4a16_gemm needs for this problem on the current device; 0 means
- * none (workspace may then be NULL).  The tensor-core path splits K across CTAs when the output
- * tiles alone would leave SMs idle; the workspace then holds 4096 bytes of per-tile arrival
- * counters at offset 0 followed by fp32 partial tiles.  Stable for given arguments on a given
- * device.  The first 4096 bytes must be zero before the first use; every call that completes
- * leaves them zero (whatever its shape), so one buffer, sized for the largest problem, serves
- * call after call.  Calls that share a workspace must not overlap on the GPU (one workspace per
- * concurrent stream).  After a device-side error, zero the first 4096 bytes again. */
+/* Bytes of device workspace w4a16_gemm needs for this problem on the current device under the
+ * current options; 0 means none (workspace may then be NULL).  The tensor-core path splits K
+ * across up to 8 CTAs when the output tiles alone would leave SMs idle, and adds the fp32
+ * partial tiles in split order.  By default the CTAs of a tile form a thread-block cluster
+ * and add them through distributed shared memory: no workspace.  The workspace reduction
+ * (W4A16_SPLITK_GLOBAL, or a GPU that cannot run the clusters) needs 4096 bytes of per-tile
+ * arrival counters at offset 0 followed by the partial tiles.  Stable for given arguments,
+ * options and device.  The first 4096 bytes must be zero before the first use; every call that
+ * completes leaves them zero (whatever its shape), so one buffer, sized for the largest
+ * problem, serves call after call.  Calls that share a workspace must not overlap on the GPU
+ * (one workspace per concurrent stream).  After a device-side error, zero the first 4096 bytes
+ * again.  Both reductions give bit-identical results. */
 size_t w4a16_workspace_bytes(int M, int N, int K, int g);
 
 /* One-time repack of AWQ tensors into the packed layout (integer-exact; scales copied bit for
@@ -137,9 +141,10 @@ int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *st
 /* y = x . W like w4a16_gemm, for callers that cannot allocate device memory at all -- a runtime
  * that plans every device buffer ahead and hands a layer only its inputs and outputs, a plugin
  * host that forbids allocation after start-up, a latency-critical path where an allocation could
- * stall or fail.  No workspace is passed: the split-K scratch of the tensor-core path lives in
- * an array of W4A16_NOALLOC_SCRATCH_BYTES inside the library (no counterpart on the pages; this
- * entry point exists only for such callers).  The caller still provides x, packed and y as for
+ * stall or fail.  No workspace is passed: when the tensor-core path adds split-K partial tiles
+ * through memory (the workspace reduction), they live in an array of
+ * W4A16_NOALLOC_SCRATCH_BYTES inside the library (no counterpart on the pages; this entry point
+ * exists only for such callers).  The caller still provides x, packed and y as for
  * w4a16_gemm.  Returns W4A16_ERR_WORKSPACE when the problem's scratch (w4a16_workspace_bytes)
  * exceeds that size.  All calls share the one array, so calls that overlap on the GPU race with
  * each other and must be serialized.  The first call on a device sets that device up
@@ -148,6 +153,16 @@ int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *st
  * cudaMalloc, cudaFree or any other allocating routine. */
 int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                        void *stream);
+
+/* Process-wide options, read by the host when a call launches its kernels. */
+#define W4A16_OPT_SPLITK_REDUCTION 1 /* how split-K partial tiles are added:              */
+#define W4A16_SPLITK_AUTO 0          /*   cluster + distributed shared memory if possible */
+#define W4A16_SPLITK_GLOBAL 1        /*   always through the caller's workspace           */
+
+/* Set an option (W4A16_OPT_*) to a value; W4A16_ERR_INVALID for an unknown option or value.
+ * Changes what w4a16_workspace_bytes reports for split-K problems: size workspaces after
+ * setting it.  Not a per-call or per-thread setting: set it before issuing work. */
+int w4a16_set_option(int option, int value);
 
 /* Static description of a status code. */
 const char *w4a16_status_string(int status);

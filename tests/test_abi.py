@@ -99,3 +99,11 @@ def test_status_strings(L):
     for s in range(-6, 1):
         assert binding.status_string(s) and "unknown" not in binding.status_string(s)
     assert "unknown" in binding.status_string(-99)
+
+
+def test_set_option_validation(L):
+    assert L.w4a16_set_option(1, 0) == binding.OK
+    assert L.w4a16_set_option(1, 1) == binding.OK
+    assert L.w4a16_set_option(1, 0) == binding.OK
+    assert L.w4a16_set_option(1, 7) == binding.ERR_INVALID
+    assert L.w4a16_set_option(99, 0) == binding.ERR_INVALID

@@ -303,8 +303,16 @@ def test_gemm_long_k_ring_refill(K, N, g, M):
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
 
 
+@pytest.fixture
+def splitk_global():
+    """The workspace reduction of split-K partial tiles for the duration of a test."""
+    w4.set_option(w4.binding.OPT_SPLITK_REDUCTION, w4.binding.SPLITK_GLOBAL)
+    yield
+    w4.set_option(w4.binding.OPT_SPLITK_REDUCTION, w4.binding.SPLITK_AUTO)
+
+
 @pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 129), ("square", 40)])
-def test_gemm_split_k_workspace_reuse(name, M):
+def test_gemm_split_k_workspace_reuse(name, M, splitk_global):
     """Where the tensor-core path splits K, one zero-filled workspace serves call after call:
     every completed call leaves its arrival counters at zero, and results are bit-identical."""
     K, N = SHAPES[name]
@@ -324,7 +332,7 @@ def test_gemm_split_k_workspace_reuse(name, M):
     assert_close(ys[0], y16)
 
 
-def test_gemm_workspace_too_small_is_rejected():
+def test_gemm_workspace_too_small_is_rejected(splitk_global):
     K, N = SHAPES["down"]
     L = Layer(K, N, 128, seed=17)
     M = 512
@@ -335,3 +343,27 @@ def test_gemm_workspace_too_small_is_rejected():
     with pytest.raises(w4.W4A16Error) as e:
         w4.gemm(x, L.packed, M, N, K, 128, workspace=small)
     assert e.value.status == w4.binding.ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 512), ("qkv", 129), ("square", 40), ("down", 64),
+                                    ("down", 17)])
+def test_gemm_split_k_cluster_matches_workspace_reduction(name, M):
+    """The cluster reduction (distributed shared memory, no workspace) and the workspace
+    reduction add the same partial tiles in the same order: bit-identical y, close to the oracle."""
+    K, N = SHAPES[name]
+    L = Layer(K, N, 128, seed=18)
+    x = inputs.make_x(M, K, seed=18)
+    assert w4.workspace_bytes(M, N, K, 128) == 0, "a GB300 runs the split-K clusters: no workspace"
+    y_cluster = L.gemm(x)
+    w4.set_option(w4.binding.OPT_SPLITK_REDUCTION, w4.binding.SPLITK_GLOBAL)
+    try:
+        need = w4.workspace_bytes(M, N, K, 128)
+        assert need > 0, "expected a split-K plan for this shape"
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev())
+        y_global = L.gemm(x, workspace=ws)
+    finally:
+        w4.set_option(w4.binding.OPT_SPLITK_REDUCTION, w4.binding.SPLITK_AUTO)
+    assert torch.equal(y_cluster.view(torch.int16), y_global.view(torch.int16))
+    assert w4.last_device_error() == 0
+    _, y16 = L.ref(x)
+    assert_close(y_cluster, y16)

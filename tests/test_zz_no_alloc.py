@@ -1,9 +1,9 @@
 """w4a16_gemm_noalloc against w4a16_gemm, through the C ABI.
 
 w4a16_gemm_noalloc serves callers that cannot allocate device memory (a runtime that plans every
-buffer ahead, a host that forbids allocation after start-up, a latency-critical path): instead of
-a caller workspace it keeps the tensor-core path's split-K scratch in an array built into the
-library.  That array is shared by every call and keeps the previous call's contents, so the
+buffer ahead, a host that forbids allocation after start-up, a latency-critical path): where the
+tensor-core path adds split-K partial tiles through memory, it keeps them in an array built into
+the library instead of a caller workspace.  That array is shared by every call and keeps the previous call's contents, so the
 results are checked on two calls in a row, against the ordinary entry point, within the same
 tolerance as the other GEMM tests.  This file is collected last on purpose.
 """
@@ -29,19 +29,26 @@ CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 512, 128), ("square", 40
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("reduction", [binding.SPLITK_AUTO, binding.SPLITK_GLOBAL])
 @pytest.mark.parametrize("name,M,g", CASES)
-def test_noalloc_matches_workspace_entry_point(name, M, g):
-    K, N = inputs.SHAPES[name]
-    L = Layer(K, N, g, seed=21)
-    x = torch.from_numpy(inputs.make_x(M, K, seed=21)).to(dev())
-    ref = w4.gemm(x, L.packed, M, N, K, g).float().cpu().numpy()
-    assert w4.workspace_bytes(M, N, K, g) <= 24 << 20  # within the built-in scratch
-    for _ in range(2):
-        y = torch.full((M, N), 3.0, dtype=torch.float16, device=dev())
-        assert _call(x, L.packed, M, N, K, g, y) == binding.OK
-        assert w4.last_device_error() == binding.OK
-        mx, mean = errors(y.float().cpu().numpy(), ref)
-        assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
+def test_noalloc_matches_workspace_entry_point(name, M, g, reduction):
+    """Under the workspace reduction the split-K shapes use the built-in scratch; under the
+    default cluster reduction they need none."""
+    w4.set_option(binding.OPT_SPLITK_REDUCTION, reduction)
+    try:
+        K, N = inputs.SHAPES[name]
+        L = Layer(K, N, g, seed=21)
+        x = torch.from_numpy(inputs.make_x(M, K, seed=21)).to(dev())
+        ref = w4.gemm(x, L.packed, M, N, K, g).float().cpu().numpy()
+        assert w4.workspace_bytes(M, N, K, g) <= 24 << 20  # within the built-in scratch
+        for _ in range(2):
+            y = torch.full((M, N), 3.0, dtype=torch.float16, device=dev())
+            assert _call(x, L.packed, M, N, K, g, y) == binding.OK
+            assert w4.last_device_error() == binding.OK
+            mx, mean = errors(y.float().cpu().numpy(), ref)
+            assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
+    finally:
+        w4.set_option(binding.OPT_SPLITK_REDUCTION, binding.SPLITK_AUTO)
 
 
 def test_noalloc_rejects_bad_arguments_on_the_host():

@@ -21,6 +21,10 @@ ERR_WORKSPACE = -4
 ERR_CUDA = -5
 ERR_DEVICE = -6
 
+OPT_SPLITK_REDUCTION = 1
+SPLITK_AUTO = 0
+SPLITK_GLOBAL = 1
+
 # name -> (argtypes, restype) of every extern "C" entry point of include/w4a16.h
 _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 SIGNATURES = {
@@ -34,6 +38,7 @@ SIGNATURES = {
     "w4a16_last_device_error": ([_P], _I),
     "w4a16_layout_version": ([], _I),
     "w4a16_gemm_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "w4a16_set_option": ([_I, _I], _I),
 }
 
 _lib = None
@@ -86,6 +91,11 @@ def _dev(t, dtype, name):
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+
+
+def set_option(option, value):
+    """Process-wide option (OPT_SPLITK_REDUCTION: SPLITK_AUTO or SPLITK_GLOBAL)."""
+    _check("w4a16_set_option", lib().w4a16_set_option(int(option), int(value)))
 
 
 def layout_version():

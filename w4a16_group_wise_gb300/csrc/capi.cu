@@ -158,5 +158,10 @@ int w4a16_last_device_error(void *stream) {
 
 int w4a16_layout_version(void) { return (int)kLayoutVersion; }
 
+int w4a16_set_option(int option, int value) {
+  if (option == W4A16_OPT_SPLITK_REDUCTION) return set_splitk_mode(value);
+  return W4A16_ERR_INVALID;
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

@@ -33,7 +33,10 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
+
+#include "../../include/w4a16.h"
 
 #include "dq.cuh"
 #include "kernels.h"
@@ -123,6 +126,29 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// As tmem_ld16 without the wait: several loads then one tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -134,10 +160,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 // --------------------------------------------------------------------------- the kernel
 
 // Split-K plan: each (n-tile, m-tile) is cut into `splits` consecutive ranges of 64-k stages.
-// With splits > 1 every CTA stores its fp32 partial tile into the workspace and the last one
-// to finish a tile (per-tile arrival counter) adds the partials in split order and writes y.
+// With splits > 1 the partial tiles are added in split order, so y does not depend on timing:
+//  - cluster: the splits of a tile form one thread-block cluster; every CTA leaves its fp32
+//    partial tile in its own shared memory and each adds a 1/splits slice of the tile from all
+//    of them through distributed shared memory;
+//  - global: every CTA stores its fp32 partial tile into the workspace and the last one to
+//    finish a tile (per-tile arrival counter) adds the partials and writes y.
 struct SplitPlan {
   int splits;
+  int cluster;           // 1: cluster reduction, 0: workspace reduction
   int stages_per_split;  // 64-k stages per split, even (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
   int *counters;         // [tiles], zero between calls
@@ -361,7 +392,75 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint8_t *tb = smem + warp * 2048;
   const int tiles = gridDim.x * gridDim.y, tile = blockIdx.y * gridDim.x + blockIdx.x;
   int fl = flags;
-  if (sp.splits > 1) {
+  if (sp.cluster) {
+    // partial tile [bm][128] fp32 in this CTA's (now idle) stage memory; the cluster is the
+    // tile's splits, rank = blockIdx.z
+    float *part = reinterpret_cast<float *>(smem);
+    if (!fl) {
+      for (int c00 = 16 * third; c00 < bm; c00 += 3 * 48) {  // three 16-column groups per wait
+        uint32_t v[3][16];
+#pragma unroll
+        for (int b = 0; b < 3; ++b)
+          if (c00 + 48 * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 48 * b), v[b]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int b = 0; b < 3; ++b)
+          if (c00 + 48 * b < bm) {
+#pragma unroll
+            for (int j2 = 0; j2 < 16; ++j2)
+              part[(c00 + 48 * b + j2) * kBN + 32 * quarter + lane] = __uint_as_float(v[b][j2]);
+          }
+      }
+    }
+    cluster_arrive();  // release: partials and flags of every CTA are visible to the cluster
+    cluster_wait();
+    int any = 0;
+    for (int z = 0; z < sp.splits; ++z) any |= (int)ld_cluster_u32(mapa_shared(&flags, (uint32_t)z));
+    if (any) {
+      if (blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, any);
+    } else {
+      constexpr int kMaxSplit = 8;
+      uint32_t base[kMaxSplit];
+#pragma unroll
+      for (int z = 0; z < kMaxSplit; ++z) base[z] = z < sp.splits ? mapa_shared(part, (uint32_t)z) : 0u;
+      const int E = bm * (kBN / 4);  // float4 pieces of the tile, 32 per row m
+      const int e0 = (int)((long)blockIdx.z * E / sp.splits), e1 = (int)((long)(blockIdx.z + 1) * E / sp.splits);
+      for (int e = e0 + threadIdx.x; e < e1; e += 2 * kThreads) {  // two pieces in flight
+        float4 v[2][kMaxSplit];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int eu = e + u * kThreads;
+          const uint32_t off = (uint32_t)((eu >> 5) * kBN + 4 * (eu & 31)) * 4u;
+#pragma unroll
+          for (int z = 0; z < kMaxSplit; ++z)
+            if (z < sp.splits && eu < e1) v[u][z] = ld_cluster_f4(base[z] + off);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int eu = e + u * kThreads;
+          if (eu >= e1) break;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);  // same order as the workspace reduction
+#pragma unroll
+          for (int z = 0; z < kMaxSplit; ++z)
+            if (z < sp.splits) {
+              acc.x += v[u][z].x;
+              acc.y += v[u][z].y;
+              acc.z += v[u][z].z;
+              acc.w += v[u][z].w;
+            }
+          const int gm = m0 + (eu >> 5), gn = n0 + 4 * (eu & 31);
+          if (gm < M && gn < N) {
+            uint2 o;
+            o.x = h2_as_u32(__floats2half2_rn(acc.x, acc.y));
+            o.y = h2_as_u32(__floats2half2_rn(acc.z, acc.w));
+            *reinterpret_cast<uint2 *>(y + (size_t)gm * N + gn) = o;
+          }
+        }
+      }
+    }
+    cluster_arrive();  // no CTA leaves while another still reads its partial
+    cluster_wait();
+  } else if (sp.splits > 1) {
     // store this split's fp32 partial tile [bm][128], then count the arrival
     float *mine = sp.partials + ((size_t)blockIdx.z * tiles + tile) * bm * kBN;
     if (!fl) {
@@ -391,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       if (threadIdx.x == 0) sp.counters[tile] = 0;  // ready for the next call
     }
   }
-  if (sp.splits > 1 && !last) {
+  if (sp.cluster || (sp.splits > 1 && !last)) {
     // nothing more to do
   } else if (fl) {
     if (threadIdx.x == 0) atomicOr(err, fl);
@@ -420,21 +519,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
   } else {
-    for (int c0 = 16 * third; c0 < bm; c0 += 48) {
-      uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, v);
-      uint16_t *th = reinterpret_cast<uint16_t *>(tb);
+    uint16_t *th = reinterpret_cast<uint16_t *>(tb);
+    for (int c00 = 16 * third; c00 < bm; c00 += 3 * 48) {  // three 16-column groups per wait
+      uint32_t v[3][16];
 #pragma unroll
-      for (int j2 = 0; j2 < 16; ++j2) th[j2 * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j2])));
-      __syncwarp();
+      for (int b = 0; b < 3; ++b)
+        if (c00 + 48 * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 48 * b), v[b]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
-        const int pc = lane + 32 * q, j2 = pc >> 2, nn = 8 * (pc & 3);
-        const int m = m0 + c0 + j2, n = nq + nn;
-        if (m < M && n < N)
-          *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
+      for (int b = 0; b < 3; ++b) {
+        const int c0 = c00 + 48 * b;
+        if (c0 >= bm) break;
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2)
+          th[j2 * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[b][j2])));
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
+          const int pc = lane + 32 * q, j2 = pc >> 2, nn = 8 * (pc & 3);
+          const int m = m0 + c0 + j2, n = nq + nn;
+          if (m < M && n < N)
+            *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   }
   tc_fence_before();
@@ -473,16 +581,52 @@ int sm_count_tc() {
   return count[dev];
 }
 
-// Workspace of a split-K launch: kCounterBytes of per-tile arrival counters at offset 0 (zero
-// before the first call, left zero by every completed call, whatever the shape), then the fp32
-// partial tiles (no initialisation needed).
+// Workspace of a split-K launch with the workspace reduction: kCounterBytes of per-tile
+// arrival counters at offset 0 (zero before the first call, left zero by every completed call,
+// whatever the shape), then the fp32 partial tiles (no initialisation needed).
 constexpr int kCounterBytes = 4096;
 constexpr int kMaxSplitTiles = kCounterBytes / 4;
+constexpr int kMaxSplits = 8;            // portable cluster size
+constexpr int kSmemLimit = 222 * 1024;   // opt-in dynamic shared memory of the kernel
 
 struct TcPlan {
   int bm, stages, tmem_cols, splits, stages_per_split, tiles;
+  bool cluster;
   size_t partial_bytes;
 };
+
+std::atomic<int> g_splitk_mode{W4A16_SPLITK_AUTO};
+
+// How many clusters of `splits` CTAs of this kernel can be resident at once on the current
+// device (every configuration holds one CTA per SM); cached per device and cluster size.
+int max_clusters(int splits) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplits + 1];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || splits < 1 || splits > kMaxSplits) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev][splits]) {
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, 1, splits);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemLimit;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = splits;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache[dev][splits] = n > 0 ? n : -1;
+  }
+  return cache[dev][splits] > 0 ? cache[dev][splits] : 0;
+}
 
 TcPlan plan_tc(int M, int N, int K) {
   TcPlan p;
@@ -494,18 +638,27 @@ TcPlan plan_tc(int M, int N, int K) {
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
   const int KS = (K + kBK - 1) / kBK;
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
-  // four 64-k stages per split.
+  // four 64-k stages per split and at most one cluster's worth of splits.  Where the device runs
+  // clusters, all clusters of the launch must be resident at once (measured: a second wave of
+  // clusters costs more than the splits gain), so the split count is lowered until they are;
+  // both reductions use the same count, so they add the same partial tiles.
   const int sms = sm_count_tc();
+  const int mode = g_splitk_mode.load();
+  const bool clusters = max_clusters(2) > 0;
   p.splits = 1;
   if (4 * p.tiles < 3 * sms && p.tiles <= kMaxSplitTiles) {
     p.splits = sms / p.tiles;
     if (p.splits > KS / 4) p.splits = KS / 4;
+    if (p.splits > kMaxSplits) p.splits = kMaxSplits;
     if (p.splits < 1) p.splits = 1;
+    if (clusters)
+      while (p.splits > 1 && max_clusters(p.splits) < p.tiles) --p.splits;
   }
   p.stages_per_split = (KS + p.splits - 1) / p.splits;
   p.stages_per_split += p.stages_per_split & 1;  // splits start on a 128-k chunk
   p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
-  p.partial_bytes = p.splits > 1 ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
+  p.cluster = p.splits > 1 && mode != W4A16_SPLITK_GLOBAL && clusters && max_clusters(p.splits) >= p.tiles;
+  p.partial_bytes = (p.splits > 1 && !p.cluster) ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
   return p;
 }
 
@@ -513,7 +666,13 @@ TcPlan plan_tc(int M, int N, int K) {
 
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
   const TcPlan p = plan_tc(M, N, K);
-  return p.splits > 1 ? kCounterBytes + p.partial_bytes : 0;
+  return p.partial_bytes ? kCounterBytes + p.partial_bytes : 0;
+}
+
+int set_splitk_mode(int mode) {
+  if (mode != W4A16_SPLITK_AUTO && mode != W4A16_SPLITK_GLOBAL) return W4A16_ERR_INVALID;
+  g_splitk_mode.store(mode);
+  return W4A16_OK;
 }
 
 cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y, int *err,
@@ -535,15 +694,17 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
 
   SplitPlan sp;
   sp.splits = P.splits;
+  sp.cluster = P.cluster ? 1 : 0;
   sp.stages_per_split = P.stages_per_split;
-  sp.counters = P.splits > 1 ? static_cast<int *>(workspace) : nullptr;
-  sp.partials = P.splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
+  const bool global = P.partial_bytes > 0;
+  sp.counters = global ? static_cast<int *>(workspace) : nullptr;
+  sp.partials = global ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
 
   static bool configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 222 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -552,11 +713,19 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L.total + 1024;  // + alignment slack
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (P.cluster) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = P.splits;
+    na = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, static_cast<const uint8_t *>(packed), M, N, K, g,
                             num_ktiles(K), P.bm, P.stages, P.tmem_cols, sp, y, err);
 }

@@ -28,6 +28,8 @@ cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int
 cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                            int *err, void *workspace, cudaStream_t stream);
 size_t gemm_tc_workspace_bytes(int M, int N, int K);
+// W4A16_SPLITK_AUTO or W4A16_SPLITK_GLOBAL (include/w4a16.h); returns a W4A16 status.
+int set_splitk_mode(int mode);
 
 // Device address of the library's per-device error word on the current device (null on failure).
 int *device_error_word();
