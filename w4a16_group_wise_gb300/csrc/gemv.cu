@@ -250,19 +250,19 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 constexpr int kSmallRows = 4;   // rows of x per CTA in the lean variant
 constexpr int kSmallWarps = 8;
 
-template <int D, bool FACTOR>
-__global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
+template <int D, int RT, bool FACTOR>
+__global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
     uint16_t *__restrict__ y, int *err) {
   // x ring: [warp][D slots][kSmallRows rows][128 k] fp16 = 1 KB per slot
   __shared__ __align__(16) uint8_t xring[kSmallWarps][D][kSmallRows * 256];
-  __shared__ float red[kSmallWarps][4][32];
+  __shared__ float red[kSmallWarps][RT * 4][32];
   __shared__ int bad;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r8 = lane >> 2, t = lane & 3;
-  const int tile = blockIdx.x;
-  const int b = tile / 4, i = tile % 4;
+  const int tile0 = blockIdx.x * RT;  // RT row-tiles of one n-block (tiles come in fours)
+  const int b = tile0 / 4, i0 = tile0 % 4;
   const int CB = chunk_bytes(g);
   const uint8_t *body = packed + kHeaderBytes + (size_t)b * KT * CB;
   const int mine = (KT - warp + kSmallWarps - 1) / kSmallWarps;  // chunks warp, warp + 8, ...
@@ -273,15 +273,19 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
     hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g);
   }
 
-  uint4 code[D][2];
-  uint32_t scale[D], zero[D];
+  uint4 code[D][RT][2];
+  uint32_t scale[D][RT], zero[D][RT];
   auto load_w = [&](int d, int j) {
     const uint8_t *ch = body + (size_t)(warp + j * kSmallWarps) * CB;
     const uint8_t *meta = ch + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) code[d][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
-    scale[d] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
-    zero[d] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+    for (int r = 0; r < RT; ++r) {
+      const int i = i0 + r;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) code[d][r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
+      scale[d][r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
+      zero[d][r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+    }
   };
   // x rows 0..M-1 of chunk j into slot d: M * 16 pieces of 16 bytes, lane p takes pieces p, p+32..
   auto load_x = [&](int d, int j) {
@@ -293,7 +297,11 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
     }
   };
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[RT][4];
+#pragma unroll
+  for (int r = 0; r < RT; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 #pragma unroll
   for (int d = 0; d < D; ++d)
     if (d < mine) load_w(d, d);
@@ -313,37 +321,41 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
       if (j < mine) {
         cp_async_wait_pending<D - 1>();  // this slot's x has landed (for this lane's pieces)
         __syncwarp();                     // ... and every lane's pieces are visible
-        const ZeroBias zb0 = zero_bias(zero[d] & 0xFu), zb1 = zero_bias((zero[d] >> 4) & 0xFu);
         const uint8_t *xs = &xring[warp][d][r8 * 256 + 64 * t];
         const bool xrow = r8 < M;
-        float dd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t w0 = (w == 0) ? code[d][0].x : (w == 1) ? code[d][0].y : (w == 2) ? code[d][0].z : code[d][0].w;
-          const uint32_t w1 = (w == 0) ? code[d][1].x : (w == 1) ? code[d][1].y : (w == 2) ? code[d][1].z : code[d][1].w;
-          uint32_t v0[4], v1[4];
-          word_to_qz(w0, zb0, v0);
-          word_to_qz(w1, zb1, v1);
-          if (!FACTOR) {
-            const uint32_t s20 = (scale[d] & 0xFFFFu) * 0x00010001u, s21 = (scale[d] >> 16) * 0x00010001u;
+        for (int r = 0; r < RT; ++r) {
+          const ZeroBias zb0 = zero_bias(zero[d][r] & 0xFu), zb1 = zero_bias((zero[d][r] >> 4) & 0xFu);
+          float dd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v0[e] = hmul2_u32(v0[e], s20);
-              v1[e] = hmul2_u32(v1[e], s21);
+          for (int w = 0; w < 4; ++w) {
+            const uint4 c0 = code[d][r][0], c1 = code[d][r][1];
+            const uint32_t w0 = (w == 0) ? c0.x : (w == 1) ? c0.y : (w == 2) ? c0.z : c0.w;
+            const uint32_t w1 = (w == 0) ? c1.x : (w == 1) ? c1.y : (w == 2) ? c1.z : c1.w;
+            uint32_t v0[4], v1[4];
+            word_to_qz(w0, zb0, v0);
+            word_to_qz(w1, zb1, v1);
+            if (!FACTOR) {
+              const uint32_t s20 = (scale[d][r] & 0xFFFFu) * 0x00010001u, s21 = (scale[d][r] >> 16) * 0x00010001u;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v0[e] = hmul2_u32(v0[e], s20);
+                v1[e] = hmul2_u32(v1[e], s21);
+              }
             }
+            const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
+            float *dst = FACTOR ? dd : acc[r];
+            mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+            mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
           }
-          const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
-          float *dst = FACTOR ? dd : acc;
-          mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
-          mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
-        }
-        if (FACTOR) {
-          const float f0 = __half2float(__ushort_as_half((unsigned short)(scale[d] & 0xFFFFu)));
-          const float f1 = __half2float(__ushort_as_half((unsigned short)(scale[d] >> 16)));
-          acc[0] = fmaf(f0, dd[0], acc[0]);
-          acc[1] = fmaf(f0, dd[1], acc[1]);
-          acc[2] = fmaf(f1, dd[2], acc[2]);
-          acc[3] = fmaf(f1, dd[3], acc[3]);
+          if (FACTOR) {
+            const float f0 = __half2float(__ushort_as_half((unsigned short)(scale[d][r] & 0xFFFFu)));
+            const float f1 = __half2float(__ushort_as_half((unsigned short)(scale[d][r] >> 16)));
+            acc[r][0] = fmaf(f0, dd[0], acc[r][0]);
+            acc[r][1] = fmaf(f0, dd[1], acc[r][1]);
+            acc[r][2] = fmaf(f1, dd[2], acc[r][2]);
+            acc[r][3] = fmaf(f1, dd[3], acc[r][3]);
+          }
         }
         __syncwarp();  // every lane is done reading the slot before it is refilled
         if (j + D < mine) {
@@ -356,19 +368,21 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 4) gemv_small_kernel(
   }
 
 #pragma unroll
-  for (int c = 0; c < 4; ++c) red[warp][c][lane] = acc[c];
+  for (int r = 0; r < RT; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) red[warp][4 * r + c][lane] = acc[r][c];
   if (threadIdx.x == 0) bad = !hdr_ok;
   __syncthreads();
   if (bad) {
     if (threadIdx.x == 0) atomicOr(err, 1);
     return;
   }
-  if (threadIdx.x < 128) {
-    const int ln = threadIdx.x % 32, c = threadIdx.x / 32;
+  if (threadIdx.x < RT * 128) {
+    const int ln = threadIdx.x % 32, c = (threadIdx.x / 32) % 4, r = threadIdx.x / 128;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kSmallWarps; ++w) v += red[w][c][ln];
-    const int row = 16 * i + (ln >> 2) + 8 * (c >> 1);
+    for (int w = 0; w < kSmallWarps; ++w) v += red[w][4 * r + c][ln];
+    const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
     if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(v));
@@ -425,11 +439,11 @@ cudaError_t launch_rt(int tiles, int mblocks, int W, int MB, bool factor, const 
                 : launch_variant<RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
 }
 
-template <int D>
+template <int D, int RT>
 cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
                          int KT, uint16_t *y, int *err, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles);
+  cfg.gridDim = dim3((tiles + RT - 1) / RT);
   cfg.blockDim = dim3(32 * kSmallWarps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -438,8 +452,8 @@ cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, true>, x, p, M, N, K, g, KT, y, err)
-                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, false>, x, p, M, N, K, g, KT, y, err);
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, RT, true>, x, p, M, N, K, g, KT, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, RT, false>, x, p, M, N, K, g, KT, y, err);
 }
 
 }  // namespace
@@ -456,7 +470,12 @@ cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int
   const long ctas1 = (long)tiles * mblocks;
   // Lean variant for M <= 4 unless K is long and the grid is small (then 16 warps per CTA win).
   const bool long_k = KT >= 32 && ctas1 <= sm_count();
-  if (M <= kSmallRows && !long_k) return launch_small<2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+  if (M <= kSmallRows && !long_k) {
+    // one-tile CTAs (4 per SM) while they fit in one wave; two-tile CTAs (3 per SM) beyond, so
+    // that every CTA is resident and has issued all its weight loads when the wait ends
+    if (ctas1 <= 4L * sm_count()) return launch_small<2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+    return launch_small<2, 2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+  }
   // Two row-tiles per CTA once the grid would cover the GPU several times over (a 2-tile CTA
   // never straddles an n-block: tiles come in fours per n-block and pairs start at even tiles);
   // with 16 rows of x the per-CTA weights are reused twice as often, so earlier.  Four warps on
