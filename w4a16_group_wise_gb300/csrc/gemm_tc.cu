@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -50,9 +51,13 @@ constexpr int kBN = 128;                      // weight rows (output columns n) 
 constexpr int kBK = 64;                       // k per stage: one 128-byte swizzle atom of fp16
 constexpr int kAStageBytes = kBN * kBK * 2;   // 16 KB
 constexpr int kMaxStages = 6;
-constexpr int kThreads = 384;   // warp 0 x TMA, warp 1 MMA, warp 2 code copies, warps 4..11 dequant
+// warp 0 x TMA, warp 1 MMA, warp 2 code copies, warps 4..11 dequant, warps 12..15 epilogue of a
+// persistent CTA
+constexpr int kThreads = 512;
 constexpr int kDeqThreads = 256;
 constexpr int kDeqWarps = kDeqThreads / 32;
+constexpr int kEpiWarps = 4;
+constexpr int kGroups = kThreads / 128;  // warps per TMEM lane quarter
 constexpr int kCodeSlots = 3;         // 128-k chunks of codes in flight
 constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 160) at g = 32
 
@@ -169,6 +174,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 struct SplitPlan {
   int splits;
   int cluster;           // 1: cluster reduction, 0: workspace reduction
+  int persist;           // 1: one CTA per SM walks the tiles, two accumulators (splits == 1)
+  int ntn, ntm;          // n-tiles and m-tiles of the problem
   int stages_per_split;  // 64-k stages per split, even (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
   int *counters;         // [tiles], zero between calls
@@ -184,22 +191,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
   __shared__ uint64_t cfull_bar[kCodeSlots], cempty_bar[kCodeSlots];
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // the two accumulators of a persistent CTA
   __shared__ uint32_t tmem_base;
   __shared__ int flags, last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmSmem L = gemm_smem(bm, stages);
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bm;
   const int NB = num_nblocks(N);
   const int CB = chunk_bytes(g);
   const int KS = (K + kBK - 1) / kBK;  // 64-k stages over K (a padded half chunk is skipped)
   const int st_begin = blockIdx.z * sp.stages_per_split;  // even: a split starts on a chunk
   const int nst = max(0, min(KS, st_begin + sp.stages_per_split) - st_begin);
-  const int nch = (nst + 1) / 2;  // 128-k chunks this CTA reads
+  const int nch = (nst + 1) / 2;  // 128-k chunks per tile
   const uint32_t x_bytes = (uint32_t)bm * kBK * 2;
-  const int nb0 = n0 >> 6;                      // first n-block of the tile
-  const int nblk = (nb0 + 1 < NB) ? 2 : 1;      // the last tile may hold one n-block only
   uint8_t *codes = smem + L.codes_off;
+  // Tiles of this CTA: a persistent CTA takes tiles blockIdx.x, + gridDim.x, ... of the
+  // (n-tile, m-tile) grid (m fastest, so neighbouring CTAs share weights); otherwise the one
+  // tile (blockIdx.x, blockIdx.y).
+  const int ntiles = sp.ntn * sp.ntm;
+  const int my_tiles = sp.persist ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  auto tile_n0 = [&](int it) {
+    return (sp.persist ? ((int)blockIdx.x + it * (int)gridDim.x) / sp.ntm : (int)blockIdx.x) * kBN;
+  };
+  auto tile_m0 = [&](int it) {
+    return (sp.persist ? ((int)blockIdx.x + it * (int)gridDim.x) % sp.ntm : (int)blockIdx.y) * bm;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -210,8 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mbar_init(&cfull_bar[c], 1);             // expect-tx arrival of the bulk copies
       mbar_init(&cempty_bar[c], kDeqWarps);    // every dequant warp is done reading the slot
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);             // one tcgen05.commit per tile
+      mbar_init(&tempty_bar[b], kEpiWarps);    // every epilogue warp has read the accumulator
+    }
     mbar_init(&accum_bar, 1);
-    flags = 0;
+    // the packed buffer must match the call (read-only: no need to wait for the previous kernel)
+    const Header *h = reinterpret_cast<const Header *>(packed);
+    flags = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {  // the whole warp allocates tensor memory: tmem_cols fp32 columns x 128 lanes
@@ -225,26 +247,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   griddep_launch_dependents();
+  const bool run = flags == 0;  // a header mismatch writes nothing (same in every CTA)
 
-  if (warp == 0) {
+  if (!run) {
+    // nothing to do
+  } else if (warp == 0) {
     // ------------------------------------------------------------ x tiles by TMA (one lane)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
       griddep_wait();  // x may be the previous kernel's output
       bool ok = true;
       int issued = 0;
-      for (int j = 0; j < nst; ++j) {
-        const int s = j % stages, use = j / stages;
-        if (use > 0 && !(ok = mbar_wait_sleep_bounded(&empty_bar[s], (use - 1) & 1))) break;
-        mbar_arrive_expect_tx(&full_bar[s], x_bytes);
-        tma_load_2d(smem + s * L.stage_bytes + L.b_off, &xmap, (st_begin + j) * kBK, m0, &full_bar[s]);
-        ++issued;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int m0 = tile_m0(it);
+        for (int j = 0; j < nst; ++j) {
+          const int J = it * nst + j, s = J % stages, use = J / stages;
+          if (use > 0 && !(ok = mbar_wait_sleep_bounded(&empty_bar[s], (use - 1) & 1))) break;
+          mbar_arrive_expect_tx(&full_bar[s], x_bytes);
+          tma_load_2d(smem + s * L.stage_bytes + L.b_off, &xmap, (st_begin + j) * kBK, m0, &full_bar[s]);
+          ++issued;
+        }
       }
       if (!ok) {
         atomicOr(&flags, 2);
         // let every issued copy land before the CTA may exit
-        for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
-          mbar_wait_bounded(&full_bar[j % stages], (j / stages) & 1);
+        for (int J = (issued > stages ? issued - stages : 0); J < issued; ++J)
+          mbar_wait_bounded(&full_bar[J % stages], (J / stages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -252,20 +280,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(bm);
       bool ok = true;
-      for (int j = 0; j < nst; ++j) {
-        const int s = j % stages, use = j / stages;
-        if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int ab = sp.persist ? (it & 1) : 0, ause = it >> 1;  // accumulator buffer and its use
+        if (sp.persist && ause > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[ab], (ause - 1) & 1))) break;
         tc_fence_after();
-        const uint8_t *a = smem + s * L.stage_bytes + L.a_off;
-        const uint8_t *b = smem + s * L.stage_bytes + L.b_off;
+        const uint32_t acc = tmem + (uint32_t)(ab * bm);
+        for (int j = 0; j < nst; ++j) {
+          const int J = it * nst + j, s = J % stages, use = J / stages;
+          if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
+          tc_fence_after();
+          const uint8_t *a = smem + s * L.stage_bytes + L.a_off;
+          const uint8_t *b = smem + s * L.stage_bytes + L.b_off;
 #pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks)  // 32 bytes of each 128-byte row per MMA
-          mma_f16(tmem, sw128_desc(a + 32 * ks), sw128_desc(b + 32 * ks), idesc, (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+          for (int ks = 0; ks < kBK / 16; ++ks)  // 32 bytes of each 128-byte row per MMA
+            mma_f16(acc, sw128_desc(a + 32 * ks), sw128_desc(b + 32 * ks), idesc, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+        }
+        if (!ok) break;
+        // the accumulator is final once every MMA above completes
+        mma_commit(sp.persist ? &tfull_bar[ab] : &accum_bar);
       }
-      if (!ok) atomicOr(&flags, 2);
-      mma_commit(&accum_bar);  // the accumulator is final once every MMA above completes
-      if (!mbar_wait_sleep_bounded(&accum_bar, 0)) atomicOr(&flags, 2);
+      if (!ok) {  // let every issued MMA finish before the CTA may exit
+        atomicOr(&flags, 2);
+        mma_commit(&accum_bar);
+        mbar_wait_sleep_bounded(&accum_bar, 0);
+      } else if (!sp.persist && !mbar_wait_sleep_bounded(&accum_bar, 0)) {
+        atomicOr(&flags, 2);
+      }
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ packed chunks by bulk copy
@@ -273,31 +314,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (lane == 0) {
       bool ok = true;
       int issued = 0;
-      for (int lc = 0; lc < nch; ++lc) {
-        const int cs = lc % kCodeSlots, use = lc / kCodeSlots;
-        if (use > 0 && !(ok = mbar_wait_sleep_bounded(&cempty_bar[cs], (use - 1) & 1))) break;
-        const int c = (st_begin >> 1) + lc;
-        mbar_arrive_expect_tx(&cfull_bar[cs], (uint32_t)(nblk * CB));
-        for (int q = 0; q < nblk; ++q)
-          bulk_load(codes + cs * kCodeSlotBytes + q * CB,
-                    packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + c) * CB, (uint32_t)CB, &cfull_bar[cs]);
-        ++issued;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int nb0 = tile_n0(it) >> 6;
+        const int nblk = (nb0 + 1 < NB) ? 2 : 1;  // the last n-tile may hold one n-block only
+        for (int lc = 0; lc < nch; ++lc) {
+          const int LC = it * nch + lc, cs = LC % kCodeSlots, use = LC / kCodeSlots;
+          if (use > 0 && !(ok = mbar_wait_sleep_bounded(&cempty_bar[cs], (use - 1) & 1))) break;
+          const int c = (st_begin >> 1) + lc;
+          mbar_arrive_expect_tx(&cfull_bar[cs], (uint32_t)(nblk * CB));
+          for (int q = 0; q < nblk; ++q)
+            bulk_load(codes + cs * kCodeSlotBytes + q * CB,
+                      packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + c) * CB, (uint32_t)CB, &cfull_bar[cs]);
+          ++issued;
+        }
       }
       if (!ok) atomicOr(&flags, 2);
       // every issued copy has landed before the CTA may exit (at once in the normal case)
-      for (int lc = (issued > kCodeSlots ? issued - kCodeSlots : 0); lc < issued; ++lc)
-        mbar_wait_bounded(&cfull_bar[lc % kCodeSlots], (lc / kCodeSlots) & 1);
+      for (int LC = (issued > kCodeSlots ? issued - kCodeSlots : 0); LC < issued; ++LC)
+        mbar_wait_bounded(&cfull_bar[LC % kCodeSlots], (LC / kCodeSlots) & 1);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ------------------------------------------------------------ dequant producers
-    // Two groups of four warps take alternate 64-k stages (group gsel: stages gsel, gsel + 2,
-    // ...), so two stages are converted at once.  In a group, lane l of warp w converts
-    // column-row r = 32 (w % 4) + l: the 64 k of the stage are 32 code bytes of the row in the
-    // chunk slot (read one stage ahead, before the waits, to hide the shared-memory latency),
-    // giving eight 16-byte pieces of the swizzled A row.
+    // Two groups of four warps take alternate 64-k stages of every tile (group gsel: stages
+    // gsel, gsel + 2, ...), so two stages are converted at once.  In a group, lane l of warp w
+    // converts column-row r = 32 (w % 4) + l: the 64 k of the stage are 32 code bytes of the
+    // row in the chunk slot (read one stage ahead, before the waits, to hide the shared-memory
+    // latency), giving eight 16-byte pieces of the swizzled A row.  A persistent CTA's tiles
+    // have an even number of stages, so every chunk is read by both groups.
     const int gsel = (warp - 4) >> 2;
     const int r = 32 * (warp & 3) + lane;
-    const bool have = nb0 + (r >> 6) < NB;        // the last tile may hold one n-block only
     const int rr = r & 63;                        // row inside the n-block
     const int p = meta_pos(rr);
     const int rot = (rr >> 1) & 1;                // read order of the two 16-byte halves (banks)
@@ -305,8 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint4 h[2];                                 // k 0..31 and 32..63 of the stage
       uint32_t sc[2], zw[2];                      // scale and zero word of each 32-k half
     };
-    auto read_codes = [&](int j, Codes &cd) {
-      const int cs = (j >> 1) % kCodeSlots;
+    // read stage j of tile it (global chunk it * nch + j / 2)
+    auto read_codes = [&](int it, int j, Codes &cd) {
+      const int cs = (it * nch + (j >> 1)) % kCodeSlots;
+      const bool have = (tile_n0(it) >> 6) + (r >> 6) < NB;          // the last n-tile may hold one n-block
       const uint8_t *ch = codes + cs * kCodeSlotBytes + (r >> 6) * CB;  // this row's chunk copy
       const int k64 = (st_begin + j) & 1;                              // stage half of the chunk
       uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;                      // read 0: half rot, read 1: the other
@@ -329,14 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       cd.zw[0] = rot ? z1 : z0;
       cd.zw[1] = rot ? z0 : z1;
     };
+    auto wait_codes = [&](int it, int j) {
+      const int LC = it * nch + (j >> 1);
+      return mbar_wait_bounded(&cfull_bar[LC % kCodeSlots], (LC / kCodeSlots) & 1);
+    };
     bool ok = true;
     Codes cur;
-    if (gsel < nst) {
-      ok = mbar_wait_bounded(&cfull_bar[(gsel >> 1) % kCodeSlots], ((gsel >> 1) / kCodeSlots) & 1);
-      if (ok) read_codes(gsel, cur);
+    int it = 0, j = gsel;
+    if (j >= nst) it = my_tiles;  // this group has no stage (one-stage split)
+    if (it < my_tiles) {
+      ok = wait_codes(it, j);
+      if (ok) read_codes(it, j, cur);
     }
-    for (int j = gsel; j < nst && ok; j += 2) {
-      const int s = j % stages, use = j / stages;
+    while (it < my_tiles && ok) {
+      const int J = it * nst + j, s = J % stages, use = J / stages;
       // convert this stage's codes into registers
       uint4 out[8];
 #pragma unroll
@@ -354,12 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       // every lane has its codes in registers: this group is done with the chunk's slot
       __syncwarp();
-      if (lane == 0) mbar_arrive(&cempty_bar[(j >> 1) % kCodeSlots]);
-      // read the next stage of this group (the next chunk) while waiting for the stage buffer
-      const int jn = j + 2;
-      if (jn < nst) {
-        if (!(ok = mbar_wait_bounded(&cfull_bar[(jn >> 1) % kCodeSlots], ((jn >> 1) / kCodeSlots) & 1))) break;
-        read_codes(jn, cur);
+      if (lane == 0) mbar_arrive(&cempty_bar[(it * nch + (j >> 1)) % kCodeSlots]);
+      // the group's next stage (the next chunk, or the first of the next tile): read it while
+      // waiting for the stage buffer
+      int itn = it, jn = j + 2;
+      if (jn >= nst) {
+        ++itn;
+        jn = gsel;
+      }
+      if (itn < my_tiles) {
+        if (!(ok = wait_codes(itn, jn))) break;
+        read_codes(itn, jn, cur);
       }
       if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
       uint8_t *a = smem + s * L.stage_bytes + L.a_off + r * 128;
@@ -368,25 +426,69 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(&full_bar[s]);
+      it = itn;
+      j = jn;
+    }
+    if (!ok) atomicOr(&flags, 2);
+  } else if (warp >= 4 + kDeqWarps && sp.persist) {
+    // ------------------------------------------------------------ persistent epilogue
+    // Warp q of the four reads TMEM lanes 32q .. 32q + 31 (column-rows n) of an accumulator
+    // while the MMAs fill the other one; lane pairs swap halves so that each lane stores two
+    // consecutive n of one row m.
+    const int q = warp & 3;
+    griddep_wait();  // y may still be read by the previous kernel
+    bool ok = true;
+    for (int it = 0; it < my_tiles && ok; ++it) {
+      const int ab = it & 1, ause = it >> 1;
+      if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[ab], ause & 1))) break;
+      tc_fence_after();
+      const int n0 = tile_n0(it), m0 = tile_m0(it);
+      const int n = n0 + 32 * q + (lane & ~1);
+      const bool odd = lane & 1;
+      const bool store = flags == 0;
+      for (int c00 = 0; c00 < bm; c00 += 64) {  // four 16-column groups per wait
+        uint32_t v[4][16];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (c00 + 16 * b < bm)
+            tmem_ld16_async(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * bm + c00 + 16 * b), v[b]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (c00 + 16 * b >= bm) break;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t u = h2_as_u32(__floats2half2_rn(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1])));
+            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, u, 1);
+            // even lane: row m_{2i} = (own, neighbour) low halves; odd lane: row m_{2i+1} high halves
+            const uint32_t w = odd ? __byte_perm(o, u, 0x7632) : __byte_perm(u, o, 0x5410);
+            const int m = m0 + c00 + 16 * b + 2 * i + (odd ? 1 : 0);
+            if (store && m < M && n < N) *reinterpret_cast<uint32_t *>(y + (size_t)m * N + n) = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[ab]);  // the MMAs may refill this accumulator
     }
     if (!ok) atomicOr(&flags, 2);
   }
 
-  // ------------------------------------------------------------ epilogue (all warps)
-  // Only the MMA lane waits for the accumulator (above); every other thread parks in the
-  // hardware barrier below instead of polling, so the producers keep the issue slots.
+  // ------------------------------------------------------------ end of a persistent CTA, or
+  // the epilogue of a one-tile CTA (all warps).  Only the MMA lane waits for a one-tile CTA's
+  // accumulator (above); every other thread parks in the hardware barrier below instead of
+  // polling, so the producers keep the issue slots.
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (sp.persist || !run) {
+    if (threadIdx.x == 0 && flags) atomicOr(err, flags);
+  } else {
   griddep_wait();  // every storing thread waits for the previous kernel (a no-op once satisfied)
-  if (threadIdx.x == 0) {
-    const Header *h = reinterpret_cast<const Header *>(packed);
-    if (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g) atomicOr(&flags, 1);
-  }
-  __syncthreads();
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bm;
   // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (column-rows n) and the 16-column groups c of the
-  // tile with c % 3 == w / 4; a per-warp 2 KB transpose buffer in the (now idle) stage memory
-  // turns each group into 16-byte stores of consecutive n.
+  // tile with c % kGroups == w / 4; a per-warp 2 KB transpose buffer in the (now idle) stage
+  // memory turns each group into 16-byte stores of consecutive n.
   const int quarter = warp & 3, third = warp >> 2;
   const int nq = n0 + 32 * quarter;  // first column-row of this warp
   uint8_t *tb = smem + warp * 2048;
@@ -397,18 +499,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // tile's splits, rank = blockIdx.z
     float *part = reinterpret_cast<float *>(smem);
     if (!fl) {
-      for (int c00 = 16 * third; c00 < bm; c00 += 3 * 48) {  // three 16-column groups per wait
+      for (int c00 = 16 * third; c00 < bm; c00 += 3 * 16 * kGroups) {  // three 16-column groups per wait
         uint32_t v[3][16];
 #pragma unroll
         for (int b = 0; b < 3; ++b)
-          if (c00 + 48 * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 48 * b), v[b]);
+          if (c00 + 16 * kGroups * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 16 * kGroups * b), v[b]);
         tmem_wait_ld();
 #pragma unroll
         for (int b = 0; b < 3; ++b)
-          if (c00 + 48 * b < bm) {
+          if (c00 + 16 * kGroups * b < bm) {
 #pragma unroll
             for (int j2 = 0; j2 < 16; ++j2)
-              part[(c00 + 48 * b + j2) * kBN + 32 * quarter + lane] = __uint_as_float(v[b][j2]);
+              part[(c00 + 16 * kGroups * b + j2) * kBN + 32 * quarter + lane] = __uint_as_float(v[b][j2]);
           }
       }
     }
@@ -464,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // store this split's fp32 partial tile [bm][128], then count the arrival
     float *mine = sp.partials + ((size_t)blockIdx.z * tiles + tile) * bm * kBN;
     if (!fl) {
-      for (int c0 = 16 * third; c0 < bm; c0 += 48) {
+      for (int c0 = 16 * third; c0 < bm; c0 += 16 * kGroups) {
         uint32_t v[16];
         tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -496,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (threadIdx.x == 0) atomicOr(err, fl);
   } else if (sp.splits > 1) {
     // add the partials in split order, 4 consecutive n per piece
-    for (int c0 = 16 * third; c0 < bm; c0 += 48) {
+    for (int c0 = 16 * third; c0 < bm; c0 += 16 * kGroups) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int pc = lane + 32 * q, j2 = pc >> 3, nn = 4 * (pc & 7);
@@ -520,15 +622,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   } else {
     uint16_t *th = reinterpret_cast<uint16_t *>(tb);
-    for (int c00 = 16 * third; c00 < bm; c00 += 3 * 48) {  // three 16-column groups per wait
+    for (int c00 = 16 * third; c00 < bm; c00 += 3 * 16 * kGroups) {  // three 16-column groups per wait
       uint32_t v[3][16];
 #pragma unroll
       for (int b = 0; b < 3; ++b)
-        if (c00 + 48 * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 48 * b), v[b]);
+        if (c00 + 16 * kGroups * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 16 * kGroups * b), v[b]);
       tmem_wait_ld();
 #pragma unroll
       for (int b = 0; b < 3; ++b) {
-        const int c0 = c00 + 48 * b;
+        const int c0 = c00 + 16 * kGroups * b;
         if (c0 >= bm) break;
 #pragma unroll
         for (int j2 = 0; j2 < 16; ++j2)
@@ -545,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
   }
+  }  // one-tile epilogue
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -591,7 +694,7 @@ constexpr int kSmemLimit = 222 * 1024;   // opt-in dynamic shared memory of the 
 
 struct TcPlan {
   int bm, stages, tmem_cols, splits, stages_per_split, tiles;
-  bool cluster;
+  bool cluster, persist;
   size_t partial_bytes;
 };
 
@@ -633,8 +736,7 @@ TcPlan plan_tc(int M, int N, int K) {
   p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
   p.stages = 0;
   while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 220 * 1024) ++p.stages;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < p.bm) p.tmem_cols *= 2;
+  p.tmem_cols = 32;  // set below, once the split is known
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
   const int KS = (K + kBK - 1) / kBK;
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
@@ -659,6 +761,10 @@ TcPlan plan_tc(int M, int N, int K) {
   p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
   p.cluster = p.splits > 1 && mode != W4A16_SPLITK_GLOBAL && clusters && max_clusters(p.splits) >= p.tiles;
   p.partial_bytes = (p.splits > 1 && !p.cluster) ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
+  // Without a split, one CTA per SM walks the tiles with two accumulators, so that a tile's
+  // epilogue overlaps the next tile's MMAs (tiles then need an even number of stages)
+  p.persist = p.splits == 1 && KS % 2 == 0;
+  while (p.tmem_cols < (p.persist ? 2 : 1) * p.bm) p.tmem_cols *= 2;
   return p;
 }
 
@@ -696,6 +802,9 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   sp.splits = P.splits;
   sp.cluster = P.cluster ? 1 : 0;
   sp.stages_per_split = P.stages_per_split;
+  sp.persist = P.persist ? 1 : 0;
+  sp.ntn = (N + kBN - 1) / kBN;
+  sp.ntm = (M + P.bm - 1) / P.bm;
   const bool global = P.partial_bytes > 0;
   sp.counters = global ? static_cast<int *>(workspace) : nullptr;
   sp.partials = global ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
@@ -709,7 +818,7 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((N + kBN - 1) / kBN, (M + P.bm - 1) / P.bm, P.splits);
+  cfg.gridDim = P.persist ? dim3(std::min(P.tiles, sm_count_tc())) : dim3(sp.ntn, sp.ntm, P.splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L.total + 1024;  // + alignment slack
   cfg.stream = stream;
