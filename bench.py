@@ -35,10 +35,12 @@ DECODE_SHAPES = [("qkv", 2048, 3072), ("gate_up", 2048, 13312), ("down", 6656, 2
 LAYERS = 8
 METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate_up/down, g=128)"
 
-# DRAM bytes per launch of the decode kernel from the ncu capture summarised in
-# profiles/gemv_decode_ncu.md, keyed by the sha256 of the kernel source it was taken on; it
-# is reported as null whenever the source has changed since.
-TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+# DRAM bytes per launch of the decode kernel, averaged over the step's three shapes, from ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch each of q_k_v, gate_up
+# and down at M=1, summarised under profiles/), keyed by the sha256 of the kernel source they
+# were taken on; reported as null whenever that source has changed since.
+TRAFFIC = {"source_sha256": "e6b55834a0f5650c1623187112580a7456dc7889b69fcf2c9cfe18cd01672c4b",
+           "bytes_per_launch": (3299072 + 14200832 + 7119872) // 3}
 
 
 def alg_bytes(M, K, N, g=G):
