@@ -4,31 +4,36 @@
 // activations is linear in the batch (12.9x slower than bf16 at 512 rows), so wide batches
 // unpack the weight once and run an ordinary dense GEMM (vllm-omni commit "Add cpu_int4, an
 // asymmetric 4-bit weight path for vLLM's CPU backend").  Here the unpacking is fused into the
-// GEMM: each 128 x 128 weight tile is dequantized once per CTA into shared memory and consumed
+// GEMM: each 128 x 64 weight tile is dequantized once per CTA into tensor memory and consumed
 // by the 5th-generation tensor cores (tcgen05.mma, fp16 x fp16 -> fp32 in tensor memory); no
 // dequantized W ever reaches HBM.
 //
 // Orientation: D[n][m] = sum_k W^T[n][k] * x^T[k][m], i.e. the MMA's M dimension (128) runs
 // over output columns n and its N dimension (BM <= 256) over rows m of x, so few rows of x
-// waste no tensor work.  Roles:
+// waste no tensor work.  Roles, per 64-k stage of a ring of up to 8 stages:
 //  - one lane of warp 2 copies the packed chunks of the tile's two n-blocks (codes and their
 //    scales and zeros, contiguous in the packed layout) into a ring of shared-memory slots with
 //    bulk asynchronous copies, one 128-k chunk per slot;
-//  - one lane of warp 0 loads the x tile of each 64-k stage (BM rows x 64 k, fp16) with a TMA
-//    copy into a 128-byte-swizzled K-major tile (rows past M and k past K read as 0);
+//  - one lane of warp 0 loads the x tile (BM rows x 64 k, fp16) with a TMA copy into a
+//    128-byte-swizzled K-major tile (rows past M and k past K read as 0);
 //  - warps 4..11, in two groups taking alternate stages (one lane per column-row), read the
 //    codes from the slot, convert them to the exact fp16 weights fp16((q - z) * s) (dq.cuh) and
-//    store them into the stage's A tile with the same 128-byte swizzle, then fence the writes
-//    to the async proxy;
-//  - one lane of warp 1 issues 4 MMAs (K = 16 each) per stage once both operands are in place
-//    and commits them to the stage's "empty" barrier, which frees the stage when they complete.
-// Measured on GB300: one warp's stage (wait, read, convert, store, fence, arrive) is a chain of
-// about 1200 cycles, against about 700 cycles of MMAs per stage, so the warps must overlap
-// stages (two groups) and read ahead to keep the tensor cores fed.
-// After the last stage the accumulator is committed to a barrier, and all 12 warps read it
-// back (tcgen05.ld, 32 lanes x 16 columns each), round to fp16 and store y.  Every wait is
-// bounded: on a timeout the kernel records an error, drains, frees tensor memory and skips the
-// store.
+//    store them into the stage's A tile in tensor memory (tcgen05.st);
+//  - one lane of warp 1 issues 4 MMAs (K = 16 each, A from tensor memory, x from shared
+//    memory) once both operands are in place and commits them to the stage's "empty" barrier,
+//    which frees the stage when they complete.
+// Without a K split the CTAs are persistent (one per SM, walking the tiles) and warps 12..15
+// read each finished accumulator back (tcgen05.ld), round to fp16 and store y while the
+// producers run ahead on the next tile; with a K split every CTA has one tile and all warps
+// take part in adding the partial tiles.  Every wait is bounded: on a timeout the kernel
+// records an error, drains, frees tensor memory and skips the store.
+//
+// Measured on GB300 while tuning this pipeline: keeping the A tile out of shared memory lets
+// the ring hold 6 stages at BM = 256; one warp's stage chain (wait, read, convert, store,
+// arrive) takes ~1200 cycles against ~670 cycles of MMAs, hence two converting groups; the
+// MMA-issuing lane is on the critical path of every stage, so its loop does no divisions and
+// builds no descriptors; and prefetching code chunks into L2 with bulk prefetches slowed the
+// kernel once the rest was tuned (the copies compete for the same copy engine).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,8 +54,12 @@ namespace {
 
 constexpr int kBN = 128;                      // weight rows (output columns n) per CTA = MMA M
 constexpr int kBK = 64;                       // k per stage: one 128-byte swizzle atom of fp16
-constexpr int kAStageBytes = kBN * kBK * 2;   // 16 KB
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
+// Tensor memory (512 columns x 128 lanes of 32 bits): the fp32 accumulator in columns
+// [0, BM), and the stages' fp16 A tiles (128 column-rows x 64 k = 32 columns each) from
+// column kATmemCol on.
+constexpr int kTmemCols = 512;
+constexpr int kATmemCol = 256;
 // warp 0 x TMA, warp 1 MMA, warp 2 code copies, warps 4..11 dequant, warps 12..15 epilogue of a
 // persistent CTA
 constexpr int kThreads = 512;
@@ -63,19 +72,20 @@ constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 1
 
 struct GemmSmem {
   int stages, bm;
-  int a_off, b_off, stage_bytes, codes_off, total;
+  int b_off, stage_bytes, codes_off, total;
 };
 
-// [stages x (A tile, x tile)] [kCodeSlots x code slot]
+// [stages x x-tile] [kCodeSlots x code slot]; at least 32 KB (the epilogue's transpose buffers
+// reuse the front of it once the rings are idle)
 __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   GemmSmem s;
   s.bm = bm;
   s.stages = stages;
-  s.stage_bytes = kAStageBytes + bm * kBK * 2;
-  s.a_off = 0;
-  s.b_off = kAStageBytes;
+  s.stage_bytes = bm * kBK * 2;
+  s.b_off = 0;
   s.codes_off = stages * s.stage_bytes;
   s.total = s.codes_off + kCodeSlots * kCodeSlotBytes;
+  if (s.total < 32 * 1024) s.total = 32 * 1024;
   return s;
 }
 
@@ -92,12 +102,28 @@ __host__ __device__ inline uint32_t idesc_f16(int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// As mma_f16 with the A operand (128 rows x 16 k fp16, K-major) in tensor memory.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                               uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers (one lane per thread of the warp),
+// then wait until the stores are done.
+__device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -107,10 +133,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // 32 lanes x 16 consecutive 32-bit columns (one lane per thread of the warp).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -258,14 +280,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       griddep_wait();  // x may be the previous kernel's output
       bool ok = true;
       int issued = 0;
+      int s = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
         const int m0 = tile_m0(it);
         for (int j = 0; j < nst; ++j) {
-          const int J = it * nst + j, s = J % stages, use = J / stages;
           if (use > 0 && !(ok = mbar_wait_sleep_bounded(&empty_bar[s], (use - 1) & 1))) break;
           mbar_arrive_expect_tx(&full_bar[s], x_bytes);
           tma_load_2d(smem + s * L.stage_bytes + L.b_off, &xmap, (st_begin + j) * kBK, m0, &full_bar[s]);
           ++issued;
+          if (++s == stages) {
+            s = 0;
+            ++use;
+          }
         }
       }
       if (!ok) {
@@ -278,27 +304,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue (one lane)
     if (lane == 0) {
+      // This lane is on the critical path of every stage (measured: the MMAs of a stage take
+      // ~670 cycles, and a loop with per-stage divisions and descriptor builds took ~1100), so
+      // the ring position advances incrementally and the x descriptor is built once: its
+      // start-address field counts 16-byte units, so a stage adds stage_bytes / 16 and a 16-k
+      // step 2 (shared addresses stay below 256 KB, so the 14-bit field never carries).
       const uint32_t idesc = idesc_f16(bm);
+      const uint64_t bdesc0 = sw128_desc(smem + L.b_off);
+      const uint32_t bstep = (uint32_t)L.stage_bytes >> 4;
       bool ok = true;
+      int s = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
-        const int ab = sp.persist ? (it & 1) : 0, ause = it >> 1;  // accumulator buffer and its use
-        if (sp.persist && ause > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[ab], (ause - 1) & 1))) break;
+        // the accumulator is free once the epilogue warps have read the previous tile's
+        if (sp.persist && it > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[0], (it - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t acc = tmem + (uint32_t)(ab * bm);
+        const uint32_t acc = tmem;
         for (int j = 0; j < nst; ++j) {
-          const int J = it * nst + j, s = J % stages, use = J / stages;
           if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
           tc_fence_after();
-          const uint8_t *a = smem + s * L.stage_bytes + L.a_off;
-          const uint8_t *b = smem + s * L.stage_bytes + L.b_off;
-#pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks)  // 32 bytes of each 128-byte row per MMA
-            mma_f16(acc, sw128_desc(a + 32 * ks), sw128_desc(b + 32 * ks), idesc, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t a = tmem + (uint32_t)(kATmemCol + 32 * s);
+          const uint64_t bd = bdesc0 + (uint64_t)(bstep * (uint32_t)s);
+          mma_f16_tmem_a(acc, a, bd, idesc, j > 0 ? 1u : 0u);  // 16 k = 8 columns of A, 32 bytes of x
+          mma_f16_tmem_a(acc, a + 8, bd + 2, idesc, 1u);
+          mma_f16_tmem_a(acc, a + 16, bd + 4, idesc, 1u);
+          mma_f16_tmem_a(acc, a + 24, bd + 6, idesc, 1u);
           mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+          if (++s == stages) {
+            s = 0;
+            ++use;
+          }
         }
         if (!ok) break;
         // the accumulator is final once every MMA above completes
-        mma_commit(sp.persist ? &tfull_bar[ab] : &accum_bar);
+        mma_commit(sp.persist ? &tfull_bar[0] : &accum_bar);
       }
       if (!ok) {  // let every issued MMA finish before the CTA may exit
         atomicOr(&flags, 2);
@@ -312,20 +350,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------ packed chunks by bulk copy
     // (the packed weights are read-only: no need to wait for the previous kernel)
     if (lane == 0) {
+      auto chunk_src = [&](int it, int lc, int q) {
+        const int nb0 = tile_n0(it) >> 6;
+        return packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + (st_begin >> 1) + lc) * CB;
+      };
+      auto nblocks = [&](int it) { return ((tile_n0(it) >> 6) + 1 < NB) ? 2 : 1; };
       bool ok = true;
       int issued = 0;
+      int cs = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
-        const int nb0 = tile_n0(it) >> 6;
-        const int nblk = (nb0 + 1 < NB) ? 2 : 1;  // the last n-tile may hold one n-block only
+        const int nblk = nblocks(it);
         for (int lc = 0; lc < nch; ++lc) {
-          const int LC = it * nch + lc, cs = LC % kCodeSlots, use = LC / kCodeSlots;
           if (use > 0 && !(ok = mbar_wait_sleep_bounded(&cempty_bar[cs], (use - 1) & 1))) break;
-          const int c = (st_begin >> 1) + lc;
           mbar_arrive_expect_tx(&cfull_bar[cs], (uint32_t)(nblk * CB));
           for (int q = 0; q < nblk; ++q)
-            bulk_load(codes + cs * kCodeSlotBytes + q * CB,
-                      packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + c) * CB, (uint32_t)CB, &cfull_bar[cs]);
+            bulk_load(codes + cs * kCodeSlotBytes + q * CB, chunk_src(it, lc, q), (uint32_t)CB, &cfull_bar[cs]);
           ++issued;
+          if (++cs == kCodeSlots) {
+            cs = 0;
+            ++use;
+          }
         }
       }
       if (!ok) atomicOr(&flags, 2);
@@ -343,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // have an even number of stages, so every chunk is read by both groups.
     const int gsel = (warp - 4) >> 2;
     const int r = 32 * (warp & 3) + lane;
+    const int gshift = g == 32 ? 5 : g == 64 ? 6 : 7;  // group of a 32-k span: (32 k32) >> gshift
     const int rr = r & 63;                        // row inside the n-block
     const int p = meta_pos(rr);
     const int rot = (rr >> 1) & 1;                // read order of the two 16-byte halves (banks)
@@ -350,18 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint4 h[2];                                 // k 0..31 and 32..63 of the stage
       uint32_t sc[2], zw[2];                      // scale and zero word of each 32-k half
     };
-    // read stage j of tile it (global chunk it * nch + j / 2)
-    auto read_codes = [&](int it, int j, Codes &cd) {
-      const int cs = (it * nch + (j >> 1)) % kCodeSlots;
-      const bool have = (tile_n0(it) >> 6) + (r >> 6) < NB;          // the last n-tile may hold one n-block
+    // read stage j of a tile from code slot cs (have: the row's n-block exists)
+    auto read_codes = [&](int cs, bool have, int j, Codes &cd) {
       const uint8_t *ch = codes + cs * kCodeSlotBytes + (r >> 6) * CB;  // this row's chunk copy
       const int k64 = (st_begin + j) & 1;                              // stage half of the chunk
       uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;                      // read 0: half rot, read 1: the other
       uint32_t s0 = 0, s1 = 0, z0 = 0, z1 = 0;
       if (have) {
         const int ka = 2 * k64 + rot, kb = 2 * k64 + (rot ^ 1);
-        const uint8_t *ma = ch + kCodeBytes + ((32 * ka) / g) * kGroupMetaBytes;
-        const uint8_t *mb = ch + kCodeBytes + ((32 * kb) / g) * kGroupMetaBytes;
+        const uint8_t *ma = ch + kCodeBytes + ((32 * ka) >> gshift) * kGroupMetaBytes;
+        const uint8_t *mb = ch + kCodeBytes + ((32 * kb) >> gshift) * kGroupMetaBytes;
         c0 = *reinterpret_cast<const uint4 *>(ch + rr * kRowBytes + 16 * ka);
         c1 = *reinterpret_cast<const uint4 *>(ch + rr * kRowBytes + 16 * kb);
         s0 = *reinterpret_cast<const uint16_t *>(ma + 2 * p);
@@ -376,20 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       cd.zw[0] = rot ? z1 : z0;
       cd.zw[1] = rot ? z0 : z1;
     };
-    auto wait_codes = [&](int it, int j) {
-      const int LC = it * nch + (j >> 1);
-      return mbar_wait_bounded(&cfull_bar[LC % kCodeSlots], (LC / kCodeSlots) & 1);
-    };
+    auto row_has_block = [&](int it) { return (tile_n0(it) >> 6) + (r >> 6) < NB; };
     bool ok = true;
     Codes cur;
     int it = 0, j = gsel;
+    // ring positions, advanced incrementally: code slot of the current chunk and its use, stage
+    // slot of the current stage and its use (a group takes every other stage, one per chunk)
+    int cs = (j >> 1) % kCodeSlots, cuse = 0;
+    int s = j % stages, use = j / stages;
+    bool have = row_has_block(0);
     if (j >= nst) it = my_tiles;  // this group has no stage (one-stage split)
     if (it < my_tiles) {
-      ok = wait_codes(it, j);
-      if (ok) read_codes(it, j, cur);
+      ok = mbar_wait_bounded(&cfull_bar[cs], cuse & 1);
+      if (ok) read_codes(cs, have, j, cur);
     }
     while (it < my_tiles && ok) {
-      const int J = it * nst + j, s = J % stages, use = J / stages;
       // convert this stage's codes into registers
       uint4 out[8];
 #pragma unroll
@@ -407,27 +451,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       // every lane has its codes in registers: this group is done with the chunk's slot
       __syncwarp();
-      if (lane == 0) mbar_arrive(&cempty_bar[(it * nch + (j >> 1)) % kCodeSlots]);
+      if (lane == 0) mbar_arrive(&cempty_bar[cs]);
       // the group's next stage (the next chunk, or the first of the next tile): read it while
       // waiting for the stage buffer
       int itn = it, jn = j + 2;
       if (jn >= nst) {
         ++itn;
         jn = gsel;
+        if (itn < my_tiles) have = row_has_block(itn);
+      }
+      if (++cs == kCodeSlots) {
+        cs = 0;
+        ++cuse;
       }
       if (itn < my_tiles) {
-        if (!(ok = wait_codes(itn, jn))) break;
-        read_codes(itn, jn, cur);
+        if (!(ok = mbar_wait_bounded(&cfull_bar[cs], cuse & 1))) break;
+        read_codes(cs, have, jn, cur);
       }
       if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
-      uint8_t *a = smem + s * L.stage_bytes + L.a_off + r * 128;
+      tc_fence_after();  // after the MMAs that read this stage's A tile
+      {
+        // row r of the stage's A tile: lane r % 32 of the warp's lane quarter, 32 columns of
+        // consecutive k pairs
+        uint32_t v[32];
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4 *>(a + ((cc ^ (r & 7)) << 4)) = out[cc];
-      fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
+        for (int cc = 0; cc < 8; ++cc) {
+          v[4 * cc + 0] = out[cc].x;
+          v[4 * cc + 1] = out[cc].y;
+          v[4 * cc + 2] = out[cc].z;
+          v[4 * cc + 3] = out[cc].w;
+        }
+        tmem_st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kATmemCol + 32 * s), v);
+      }
+      tc_fence_before();  // the tensor cores read this tile after the barrier
       __syncwarp();
       if (lane == 0) mbar_arrive(&full_bar[s]);
       it = itn;
       j = jn;
+      if ((s += 2) >= stages) {
+        s -= stages;
+        ++use;
+      }
     }
     if (!ok) atomicOr(&flags, 2);
   } else if (warp >= 4 + kDeqWarps && sp.persist) {
@@ -439,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     griddep_wait();  // y may still be read by the previous kernel
     bool ok = true;
     for (int it = 0; it < my_tiles && ok; ++it) {
-      const int ab = it & 1, ause = it >> 1;
-      if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[ab], ause & 1))) break;
+      const int ab = 0;
+      if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[0], it & 1))) break;
       tc_fence_after();
       const int n0 = tile_n0(it), m0 = tile_m0(it);
       const int n = n0 + 32 * q + (lane & ~1);
@@ -469,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[ab]);  // the MMAs may refill this accumulator
+      if (lane == 0) mbar_arrive(&tempty_bar[0]);  // the MMAs may refill the accumulator
     }
     if (!ok) atomicOr(&flags, 2);
   }
@@ -736,7 +800,7 @@ TcPlan plan_tc(int M, int N, int K) {
   p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
   p.stages = 0;
   while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 220 * 1024) ++p.stages;
-  p.tmem_cols = 32;  // set below, once the split is known
+  p.tmem_cols = kTmemCols;
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
   const int KS = (K + kBK - 1) / kBK;
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
@@ -764,7 +828,6 @@ TcPlan plan_tc(int M, int N, int K) {
   // Without a split, one CTA per SM walks the tiles with two accumulators, so that a tile's
   // epilogue overlaps the next tile's MMAs (tiles then need an even number of stages)
   p.persist = p.splits == 1 && KS % 2 == 0;
-  while (p.tmem_cols < (p.persist ? 2 : 1) * p.bm) p.tmem_cols *= 2;
   return p;
 }
 
