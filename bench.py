@@ -15,6 +15,7 @@ Under torchrun (N > 1) every rank runs its own replica on its own GPU (the layer
 shard across GPUs here: "replicas only"); value = all ranks' bytes / the slowest rank's time.
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -236,11 +237,21 @@ def run_ours(args, rank, world, local_rank):
         ox += M * K
         oy += M * N
 
+    # every step calls the C entry point w4a16_gemm once per linear (eager launches, as a C or
+    # C++ caller would: the arguments are plain pointers prepared once), between the copies
+    gemm_c = w4.binding.lib().w4a16_gemm
+    vp = ctypes.c_void_p
+    st = vp(stream.cuda_stream)
+    e2e_args = [(vp(x.data_ptr()), vp(packed.data_ptr()), M, N, K, G, vp(y.data_ptr()), vp(0), 0, st)
+                for (_, _, K, N, packed), x, y in zip(launches, xv, yv)]
+
     def e2e_step():
         with torch.cuda.stream(stream):
             x_dev.copy_(x_host, non_blocking=True)
-            for (_, _, K, N, packed), x, y in zip(launches, xv, yv):
-                w4.gemm(x, packed, M, N, K, G, y=y, stream=stream)
+            for a in e2e_args:
+                rc = gemm_c(*a)
+                if rc != 0:
+                    raise w4.W4A16Error("w4a16_gemm", rc)
             y_host.copy_(y_dev, non_blocking=True)
 
     for _ in range(args.warmup):

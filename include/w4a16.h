@@ -117,9 +117,9 @@ int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight,
                        int K, int N, int g, int n0, int n1, void *packed, void *stream);
 
 /* y = x . W.  x fp16 bits [M][K] row-major, y fp16 bits [M][N] row-major (fully written),
- * packed from w4a16_repack with the same K, N, g.  M == 0 is a no-op.  M <= 16 takes the
+ * packed from w4a16_repack with the same K, N, g.  M == 0 is a no-op.  M <= 32 takes the
  * decode path (fused dequant + skinny GEMM streaming the packed weights once); larger M the
- * tensor-core path (weights dequantized to fp16 tile by tile in shared memory, tcgen05 MMAs
+ * tensor-core path (weights dequantized to fp16 tile by tile into tensor memory, tcgen05 MMAs
  * with fp32 accumulation in tensor memory).  Accumulation is in fp32; the result is rounded
  * once to fp16 and is bit-identical from run to run.  workspace: w4a16_workspace_bytes(M, N,
  * K, g) bytes of 16-byte aligned device memory (may be NULL when that is 0), see there.

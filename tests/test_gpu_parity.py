@@ -143,6 +143,7 @@ GEMM_CASES = [
     ("qkv", 3), ("gate_up", 8), ("down", 12),
     ("qkv", 512), ("gate_up", 512), ("down", 512),
     ("square", 17), ("square", 129),
+    ("qkv", 32), ("gate_up", 33), ("down", 40),   # either side of the decode / tensor-core switch
 ]
 
 
@@ -190,7 +191,7 @@ def test_gemm_small_ragged(K, N, g, M):
     assert_close(L.gemm(x), y16)
 
 
-@pytest.mark.parametrize("M", [1, 4, 16, 17, 130])
+@pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 130])
 @pytest.mark.parametrize("g", [32, 128])
 def test_gemm_bit_exact_when_sums_are_exact(M, g):
     """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so the result must
@@ -346,7 +347,7 @@ def test_gemm_workspace_too_small_is_rejected(splitk_global):
 
 
 @pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 512), ("qkv", 129), ("square", 40), ("down", 64),
-                                    ("down", 17)])
+                                    ("down", 40)])
 def test_gemm_split_k_cluster_matches_workspace_reduction(name, M):
     """The cluster reduction (distributed shared memory, no workspace) and the workspace
     reduction add the same partial tiles in the same order: bit-identical y, close to the oracle."""

@@ -22,7 +22,7 @@ cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W,
 cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g,
                         uint16_t *y, int *err, cudaStream_t stream);
 
-// Tensor-core path (tcgen05): y = x . W for M > 16.  `workspace` holds
+// Tensor-core path (tcgen05): y = x . W for M > kDecodeMaxM.  `workspace` holds
 // gemm_tc_workspace_bytes(M, N, K) bytes (may be null when that is 0); its counters must be zero
 // before the first call and are left zero by every completed call.
 cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
@@ -34,7 +34,9 @@ int set_splitk_mode(int mode);
 // Device address of the library's per-device error word on the current device (null on failure).
 int *device_error_word();
 
-// Largest M the decode path takes.
-constexpr int kDecodeMaxM = 16;
+// Largest M the decode path takes: the measured crossover on GB300.  In chains of 8 layers
+// the decode path was faster than the tensor-core path for every decoder shape up to M = 32
+// and slower for each of them from M = 96 (at 48 and 64 it depends on the shape).
+constexpr int kDecodeMaxM = 32;
 
 }  // namespace w4a16
