@@ -67,16 +67,19 @@ constexpr int kDeqThreads = 256;
 constexpr int kDeqWarps = kDeqThreads / 32;
 constexpr int kEpiWarps = 4;
 constexpr int kGroups = kThreads / 128;  // warps per TMEM lane quarter
-constexpr int kCodeSlots = 3;         // 128-k chunks of codes in flight
+constexpr int kMinCodeSlots = 3;      // 128-k chunks of codes in flight: at least this many,
+constexpr int kMaxCodeSlots = 12;     // and as many as the shared memory left by the x stages holds
+constexpr int kSmemBudget = 220 * 1024;
 constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 160) at g = 32
 
 struct GemmSmem {
-  int stages, bm;
+  int stages, bm, cslots;
   int b_off, stage_bytes, codes_off, total;
 };
 
-// [stages x x-tile] [kCodeSlots x code slot]; at least 32 KB (the epilogue's transpose buffers
-// reuse the front of it once the rings are idle)
+// [stages x x-tile] [cslots x code slot]; at least 32 KB (the epilogue's transpose buffers
+// reuse the front of it once the rings are idle).  Small x tiles leave room for a deeper code
+// ring: measured, the converting warps otherwise wait for the copies at small BM.
 __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   GemmSmem s;
   s.bm = bm;
@@ -84,7 +87,9 @@ __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   s.stage_bytes = bm * kBK * 2;
   s.b_off = 0;
   s.codes_off = stages * s.stage_bytes;
-  s.total = s.codes_off + kCodeSlots * kCodeSlotBytes;
+  int free_slots = (kSmemBudget - s.codes_off) / kCodeSlotBytes;
+  s.cslots = free_slots < kMinCodeSlots ? kMinCodeSlots : free_slots > kMaxCodeSlots ? kMaxCodeSlots : free_slots;
+  s.total = s.codes_off + s.cslots * kCodeSlotBytes;
   if (s.total < 32 * 1024) s.total = 32 * 1024;
   return s;
 }
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   // 1024-byte alignment of the operand tiles (the swizzle pattern repeats every 1024 bytes)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
-  __shared__ uint64_t cfull_bar[kCodeSlots], cempty_bar[kCodeSlots];
+  __shared__ uint64_t cfull_bar[kMaxCodeSlots], cempty_bar[kMaxCodeSlots];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // the two accumulators of a persistent CTA
   __shared__ uint32_t tmem_base;
   __shared__ int flags, last;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mbar_init(&full_bar[s], 1 + kDeqWarps / 2);  // TMA expect-tx arrival + one per warp of a group
       mbar_init(&empty_bar[s], 1);             // one tcgen05.commit per use
     }
-    for (int c = 0; c < kCodeSlots; ++c) {
+    for (int c = 0; c < L.cslots; ++c) {
       mbar_init(&cfull_bar[c], 1);             // expect-tx arrival of the bulk copies
       mbar_init(&cempty_bar[c], kDeqWarps);    // every dequant warp is done reading the slot
     }
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           for (int q = 0; q < nblk; ++q)
             bulk_load(codes + cs * kCodeSlotBytes + q * CB, chunk_src(it, lc, q), (uint32_t)CB, &cfull_bar[cs]);
           ++issued;
-          if (++cs == kCodeSlots) {
+          if (++cs == L.cslots) {
             cs = 0;
             ++use;
           }
@@ -374,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       if (!ok) atomicOr(&flags, 2);
       // every issued copy has landed before the CTA may exit (at once in the normal case)
-      for (int LC = (issued > kCodeSlots ? issued - kCodeSlots : 0); LC < issued; ++LC)
-        mbar_wait_bounded(&cfull_bar[LC % kCodeSlots], (LC / kCodeSlots) & 1);
+      for (int LC = (issued > L.cslots ? issued - L.cslots : 0); LC < issued; ++LC)
+        mbar_wait_bounded(&cfull_bar[LC % L.cslots], (LC / L.cslots) & 1);
     }
   } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ------------------------------------------------------------ dequant producers
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     int it = 0, j = gsel;
     // ring positions, advanced incrementally: code slot of the current chunk and its use, stage
     // slot of the current stage and its use (a group takes every other stage, one per chunk)
-    int cs = (j >> 1) % kCodeSlots, cuse = 0;
+    int cs = (j >> 1) % L.cslots, cuse = 0;
     int s = j % stages, use = j / stages;
     bool have = row_has_block(0);
     if (j >= nst) it = my_tiles;  // this group has no stage (one-stage split)
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         jn = gsel;
         if (itn < my_tiles) have = row_has_block(itn);
       }
-      if (++cs == kCodeSlots) {
+      if (++cs == L.cslots) {
         cs = 0;
         ++cuse;
       }
@@ -799,7 +804,7 @@ TcPlan plan_tc(int M, int N, int K) {
   TcPlan p;
   p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
   p.stages = 0;
-  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= 220 * 1024) ++p.stages;
+  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= kSmemBudget) ++p.stages;
   p.tmem_cols = kTmemCols;
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
   const int KS = (K + kBK - 1) / kBK;
