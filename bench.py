@@ -44,6 +44,22 @@ TRAFFIC = {"source_sha256": "e6b55834a0f5650c1623187112580a7456dc7889b69fcf2c9cf
            "bytes_per_launch": (3299072 + 14200832 + 7119872) // 3}
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank calls this with its own; one rank returns it as is."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units per second of the whole job: every rank processes `units_per_rank` (weak scaling,
+    independent replicas) within the slowest rank's `ms`."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def alg_bytes(M, K, N, g=G):
     return K * N // 2 + (K // g) * N * 5 // 2 + 2 * M * K + 2 * M * N
 
@@ -185,12 +201,7 @@ def run_ours(args, rank, world, local_rank):
             fn()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     def replay():
         with torch.cuda.stream(stream):
@@ -199,7 +210,7 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         ms = timed(replay, args.steps)
     ms_step = ms / args.steps
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_rate(step_bytes, world, ms_step) / 1e9
 
     # ---------------- per-shape kernel times (8 launches of one shape per graph replay)
     per_shape = {}
@@ -257,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         e2e_step()
     ms_e2e = timed(e2e_step, args.steps) / args.steps
-    e2e = {"value": round(step_bytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+    e2e = {"value": round(whole_job_rate(step_bytes, world, ms_e2e) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
            "ms_per_step": round(ms_e2e, 4)}
 

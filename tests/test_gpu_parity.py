@@ -171,6 +171,25 @@ def test_gemm_lm_head_sampled(M):
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
 
 
+@pytest.mark.parametrize("name,M,g", [("gate_up", 300, 128), ("gate_up", 1000, 64), ("lm_head", 200, 32)])
+def test_gemm_persistent_ragged_sampled(name, M, g):
+    """Persistent tensor-core CTAs walking several tiles each, with a ragged last m-tile (and,
+    for the LM head, hundreds of n-tiles per launch); checked on sampled outputs, every row m of
+    the last m-tile included."""
+    K, N = SHAPES[name]
+    L = Layer(K, N, g, seed=M)
+    x = inputs.make_x(M, K, seed=M)
+    y = L.gemm(x).float().cpu().numpy()
+    rng = np.random.default_rng(M)
+    mi = np.concatenate([rng.integers(0, M, 3000), np.arange(M - (M % 256 or 256), M)])
+    ni = np.concatenate([rng.integers(0, N, len(mi) - 64), np.arange(N - 64, N)])
+    ref = oracle.linear_sampled(x.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, g, mi, ni)
+    ref16 = oracle.double_to_half_bits(ref).view(np.float16).astype(np.float64)
+    mx, mean = errors(y[mi, ni], ref16)
+    assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
+    assert w4.last_device_error() == 0
+
+
 @pytest.mark.parametrize("g", [32, 64, 128])
 @pytest.mark.parametrize("M", [1, 3, 17, 129])
 @pytest.mark.parametrize("zeros", ["sym8", "uniform"])
