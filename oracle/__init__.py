@@ -50,6 +50,7 @@ def lib():
             "oracle_int4pack_cpu_chunk": ([P, I, I, I, I, P], None),
             "oracle_int4pack_cpu": ([P, I, I, P], None),
             "oracle_int4unpack_cpu": ([P, I, I, P], None),
+            "oracle_embed_gather": ([P, P, P, I, I, I, P, I, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -139,6 +140,16 @@ def dequant_f16_bits(qweight, qzeros, scales_bits, K, N, g):
     if lib().oracle_dequant_awq_f16(_p(qw), _p(qz), _p(s), K, N, g, _p(W)):
         raise MemoryError("oracle_dequant_awq_f16")
     return W
+
+
+def embed_gather(qweight, qzeros, scales_bits, K, N, g, ids):
+    """fp16 bits [T, K]: row t is column ids[t] of the dequantized W (zeros for ids outside
+    [0, N)); also returns the number of such ids."""
+    qw, qz, s = _c(qweight, np.int32), _c(qzeros, np.int32), _c(scales_bits, np.uint16)
+    ids = _c(ids, np.int32)
+    out = np.empty((len(ids), K), np.uint16)
+    bad = lib().oracle_embed_gather(_p(qw), _p(qz), _p(s), K, N, g, _p(ids), len(ids), _p(out))
+    return out, bad
 
 
 # ------------------------------------------------------------------ the linear layer

@@ -177,6 +177,43 @@ int oracle_dequant_awq_f16(const int32_t *qweight, const int32_t *qzeros, const 
     return 0;
 }
 
+/* ---------------------------------------------------------------- tied embedding -------- */
+
+/* Gather of the quantized tied embedding: the LM head's weight W [K][N] doubles as the
+ * embedding table (vllm-omni commit "cpu_int4: repack weights in n-blocks, to bound the
+ * load-time peak": "embedding 131072 x 2048 ... tied, so it is also the head"; commit "Add
+ * cpu_int4 ...": "the quantized tied embedding").  Token t reads column n = ids[t]:
+ *     out[t][k] = fp16((q[k][n] - z[k/g][n]) * s[k/g][n])     for k = 0 .. K-1,
+ * the same single rounding as the dequantized weight.  Read straight from the AWQ words: the
+ * code of column n sits in the nibble slot j with slot_to_col[j] == n % 8 of word n / 8.
+ * An id outside [0, N) gives a row of +0.  Returns the number of such ids. */
+int oracle_embed_gather(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                        int K, int N, int g, const int32_t *ids, int T, uint16_t *out) {
+    int bad = 0;
+    int slot_of_col[8];
+    for (int j = 0; j < 8; ++j) slot_of_col[awq_slot_to_col[j]] = j;
+    for (int t = 0; t < T; ++t) {
+        int n = ids[t];
+        uint16_t *row = out + (int64_t)t * K;
+        if (n < 0 || n >= N) {
+            for (int k = 0; k < K; ++k) row[k] = 0;
+            ++bad;
+            continue;
+        }
+        int word = n / 8, shift = 4 * slot_of_col[n % 8];
+        for (int k = 0; k < K; ++k) {
+            int G = k / g;
+            uint32_t qw = (uint32_t)qweight[(int64_t)k * (N / 8) + word];
+            uint32_t zw = (uint32_t)qzeros[(int64_t)G * (N / 8) + word];
+            double q = (double)((qw >> shift) & 0xFu);
+            double z = (double)((zw >> shift) & 0xFu);
+            double sv = oracle_half_to_double(scales[(int64_t)G * N + n]);
+            row[k] = oracle_double_to_half((q - z) * sv);
+        }
+    }
+    return bad;
+}
+
 /* ---------------------------------------------------------------- the linear layer ------ */
 
 /* y[m][n] = sum_{k=0}^{K-1} x[m][k] * W[k][n] in double, k summed in increasing order for

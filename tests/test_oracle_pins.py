@@ -398,3 +398,51 @@ def test_shape_orientation_and_transients():
     assert inputs.SHAPES["down"] == (6656, 2048)
     assert inputs.SHAPES["qkv"] == (2048, 3072)
     assert inputs.SHAPES["lm_head"] == (2048, 131072)
+
+
+# ------------------------------------------------------------------ tied embedding gather
+
+def _pack_awq(codes):
+    """AWQ words from codes [rows][N], written out here from the slot order of the pages'
+    packing (slot j of word c holds column 8c + (0, 2, 4, 6, 1, 3, 5, 7)[j])."""
+    rows, N = codes.shape
+    words = np.zeros((rows, N // 8), np.uint32)
+    for j, col in enumerate((0, 2, 4, 6, 1, 3, 5, 7)):
+        words |= codes[:, col::8].astype(np.uint32) << np.uint32(4 * j)
+    return words.view(np.int32)
+
+
+def test_embed_gather_closed_form():
+    """Codes q[k][n] = (k + 3n) mod 16, zero 8, scale 1: every gathered value is the small
+    integer ((k + 3n) mod 16) - 8, exact in fp16."""
+    K, N, g = 256, 96, 64
+    k = np.arange(K)[:, None]
+    n = np.arange(N)[None, :]
+    q = ((k + 3 * n) % 16).astype(np.uint8)
+    z = np.full((K // g, N), 8, np.uint8)
+    s = np.full((K // g, N), 0x3C00, np.uint16)                        # 1.0
+    ids = np.array([0, 95, 7, 8, 7, 41], np.int32)                     # duplicates and both ends
+    out, bad = oracle.embed_gather(_pack_awq(q), _pack_awq(z), s, K, N, g, ids)
+    assert bad == 0
+    want = (((np.arange(K)[None, :] + 3 * ids[:, None]) % 16) - 8).astype(np.float16)
+    assert np.array_equal(out, want.view(np.uint16))
+
+
+def test_embed_gather_matches_numpy_rounding():
+    """Random codes, zeros and scales: each gathered value is numpy's fp16 rounding of the exact
+    product (q - z) * s computed from the unpacked codes; an id outside [0, N) gives zeros."""
+    K, N, g = 384, 200, 128
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, (K // g, N)).astype(np.uint8)
+    s = rng.uniform(1e-3, 0.05, (K // g, N)).astype(np.float16)
+    ids = np.array([3, 199, -1, 120, 200, 3], np.int32)
+    out, bad = oracle.embed_gather(_pack_awq(q), _pack_awq(z), s.view(np.uint16), K, N, g, ids)
+    assert bad == 2
+    grp = np.arange(K) // g
+    for t, n in enumerate(ids):
+        if 0 <= n < N:
+            exact = (q[:, n].astype(np.float64) - z[grp, n]) * s[grp, n].astype(np.float64)
+            assert np.array_equal(out[t], exact.astype(np.float16).view(np.uint16)), t
+        else:
+            assert not out[t].any()
