@@ -274,6 +274,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- prefill M=512 (secondary): TFLOP/s of the three shapes
     prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
+    embed = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
 
     gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
     traffic = None
@@ -292,11 +293,46 @@ def run_ours(args, rank, world, local_rank):
                      "note": "achieved = algorithmic bytes of the step / step time; every launch of the step is the decode kernel"},
         "per_shape": per_shape,
         "prefill": prefill,
+        "embed": embed,
         "e2e": e2e,
         "gpu_launches": len(launches) * args.steps,
         "clocks": clk.summary(),
     }
     return result
+
+
+def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
+    """Secondary: gather of T token rows of the quantized tied embedding from the LM head
+    (K=2048, N=131072), GB/s of algorithmic bytes (codes, scale and zero per group, id, fp16 row)."""
+    K, N = inputs.SHAPES["lm_head"]
+    h = inputs.make_weights(K, N, G, seed=31)
+    packed = w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                       torch.from_numpy(h["scales"]).to(dev), K, N, G, stream=stream)
+    del h
+    ids = torch.from_numpy(np.random.default_rng(32).integers(0, N, T).astype(np.int32)).to(dev)
+    out = torch.empty((T, K), dtype=torch.float16, device=dev)
+    reps_in_graph = 10
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        w4.embed(ids, packed, K, N, G, out=out, stream=stream)
+    stream.synchronize()
+    with torch.cuda.graph(g2, stream=stream):
+        for _ in range(reps_in_graph):
+            w4.embed(ids, packed, K, N, G, out=out, stream=stream)
+    for _ in range(3):
+        g2.replay()
+
+    def rep():
+        with torch.cuda.stream(stream):
+            g2.replay()
+    reps = min(200, max(5, args.steps // 4))
+    ms = timed(rep, reps) / (reps * reps_in_graph)
+    per_token = K // 2 + (K // G) * 5 // 2 + 2 * K + 4
+    gbs = T * per_token / (ms * 1e-3) / 1e9
+    return {"metric": "tied-embedding gather GB/s (%d token rows of the %dx%d LM head, g=%d)" % (T, K, N, G),
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "peak_source": peak_src}}
 
 
 def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src):

@@ -134,6 +134,17 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
  * dequantizer. */
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream);
 
+/* Gather of the quantized tied embedding (the LM head's weight doubles as the embedding table:
+ * vllm-omni commit "cpu_int4: repack weights in n-blocks, to bound the load-time peak", whose
+ * transient table lists the embedding as "tied, so it is also the head"; commit "Add cpu_int4
+ * ...": "the quantized tied embedding").  For t < T, row t of out (fp16 bits [T][K], row-major,
+ * fully written) is column ids[t] of W: out[t][k] = fp16((q[k][n] - z[k/g][n]) * s[k/g][n]) with
+ * n = ids[t], one round-to-nearest-even rounding, bit-identical to w4a16_dequant's column n.
+ * ids: int32 [T] device array, 4-byte aligned.  T == 0 is a no-op.  An id outside [0, N) gives
+ * a row of zeros and a device-side error (w4a16_last_device_error). */
+int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                void *stream);
+
 /* Size of the scratch array built into the library for w4a16_gemm_noalloc (24 MiB): every GPU
  * that loads the library keeps this much device memory for the life of the process. */
 #define W4A16_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -107,3 +107,15 @@ def test_set_option_validation(L):
     assert L.w4a16_set_option(1, 0) == binding.OK
     assert L.w4a16_set_option(1, 7) == binding.ERR_INVALID
     assert L.w4a16_set_option(99, 0) == binding.ERR_INVALID
+
+
+def test_embed_host_validation(L):
+    # every case is rejected before any launch (the pointers are never dereferenced)
+    P4 = ctypes.c_void_p(0x10004)                                                     # 4- but not 16-byte aligned
+    assert L.w4a16_embed(P, 4, P, 2048, 2048, 100, P, NUL) == binding.ERR_UNSUPPORTED  # g
+    assert L.w4a16_embed(P, -1, P, 2048, 2048, 128, P, NUL) == binding.ERR_INVALID     # T < 0
+    assert L.w4a16_embed(NUL, 4, P, 2048, 2048, 128, P, NUL) == binding.ERR_INVALID    # ids null
+    assert L.w4a16_embed(P, 4, P, 2048, 2048, 128, NUL, NUL) == binding.ERR_INVALID    # out null
+    assert L.w4a16_embed(P, 4, P, 2048, 2048, 128, P4, NUL) == binding.ERR_MISALIGNED  # out
+    assert L.w4a16_embed(ctypes.c_void_p(0x10002), 4, P, 2048, 2048, 128, P, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_embed(NUL, 0, NUL, 2048, 2048, 128, NUL, NUL) == binding.OK          # T = 0: no-op

@@ -387,3 +387,62 @@ def test_gemm_split_k_cluster_matches_workspace_reduction(name, M):
     assert w4.last_device_error() == 0
     _, y16 = L.ref(x)
     assert_close(y_cluster, y16)
+
+
+# ------------------------------------------------------------------ tied embedding gather
+
+@pytest.mark.parametrize("name,g,T", [("lm_head", 128, 300), ("tail80", 32, 40), ("square", 64, 7)])
+def test_embed_gather_bit_exact(name, g, T):
+    """Rows of the quantized tied embedding equal the oracle's gather bit for bit: duplicate ids,
+    the first and last columns, and (N = 80) columns of the 16-wide tail n-block."""
+    K, N = SHAPES[name]
+    L = Layer(K, N, g, seed=T)
+    rng = np.random.default_rng(T)
+    ids = np.concatenate([rng.integers(0, N, T - 4), [0, N - 1, N - 1, N // 2]]).astype(np.int32)
+    if N % 64:
+        ids[:8] = np.arange(N - 16, N - 8)                    # the tail block
+    out = w4.embed(torch.from_numpy(ids).to(dev()), L.packed, K, N, g).cpu().numpy().view(np.uint16)
+    ref, bad = oracle.embed_gather(L.qweight, L.qzeros, L.scales_bits, K, N, g, ids)
+    assert bad == 0
+    assert np.array_equal(out, ref)
+    assert w4.last_device_error() == 0
+
+
+def test_embed_gather_ragged_k():
+    """K not a multiple of 128 (g = 32): the last chunk holds only part of its rows."""
+    K, N, g = 160, 192, 32
+    L = Layer(K, N, g, seed=3)
+    ids = np.array([5, 191, 64, 63, 0], np.int32)
+    out = w4.embed(torch.from_numpy(ids).to(dev()), L.packed, K, N, g).cpu().numpy().view(np.uint16)
+    ref, _ = oracle.embed_gather(L.qweight, L.qzeros, L.scales_bits, K, N, g, ids)
+    assert np.array_equal(out, ref)
+
+
+def test_embed_out_of_range_id_gives_zeros_and_an_error():
+    K, N = SHAPES["square"]
+    L = Layer(K, N, 128, seed=4)
+    ids = np.array([7, N, -3, 9], np.int32)
+    out = torch.full((4, K), 1.0, dtype=torch.float16, device=dev())
+    w4.embed(torch.from_numpy(ids).to(dev()), L.packed, K, N, 128, out=out)
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    o = out.cpu().numpy().view(np.uint16)
+    ref, bad = oracle.embed_gather(L.qweight, L.qzeros, L.scales_bits, K, N, 128, ids)
+    assert bad == 2 and np.array_equal(o, ref)
+    assert w4.last_device_error() == 0                      # the record was cleared
+
+
+def test_embed_header_mismatch_writes_nothing():
+    K, N = SHAPES["square"]
+    L = Layer(K, N, 128, seed=5)
+    ids = torch.tensor([1, 2, 3], dtype=torch.int32, device=dev())
+    out = torch.full((3, 1024), 7.0, dtype=torch.float16, device=dev())
+    w4.embed(ids, L.packed, 1024, N, 128, out=out)          # K disagrees with the packed header
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    assert bool((out == 7.0).all())
+
+
+def test_embed_empty_is_noop():
+    K, N = SHAPES["square"]
+    L = Layer(K, N, 128, seed=6)
+    out = w4.embed(torch.empty(0, dtype=torch.int32, device=dev()), L.packed, K, N, 128)
+    assert out.shape == (0, K)

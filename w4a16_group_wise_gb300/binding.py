@@ -39,6 +39,7 @@ SIGNATURES = {
     "w4a16_layout_version": ([], _I),
     "w4a16_gemm_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
     "w4a16_set_option": ([_I, _I], _I),
+    "w4a16_embed": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
 }
 
 _lib = None
@@ -181,6 +182,16 @@ def dequant(packed, K, N, g, out=None, stream=None):
     if out is None:
         out = torch.empty((K, N), dtype=torch.float16, device=packed.device)
     _check("w4a16_dequant", lib().w4a16_dequant(_ptr(packed), K, N, g, _ptr(out), _stream(stream)))
+    return out
+
+
+def embed(ids, packed, K, N, g, out=None, stream=None):
+    """Rows of the quantized tied embedding: fp16 [T, K], row t = column ids[t] of W."""
+    _dev(ids, torch.int32, "ids")
+    T = ids.numel()
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.float16, device=ids.device)
+    _check("w4a16_embed", lib().w4a16_embed(_ptr(ids), T, _ptr(packed), K, N, g, _ptr(out), _stream(stream)))
     return out
 
 

@@ -115,6 +115,19 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
   return map_launch(launch_gemm_tc(x, packed, M, N, K, g, y, err, workspace, s));
 }
 
+int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (T < 0) return W4A16_ERR_INVALID;
+  if (T == 0) return W4A16_OK;
+  if (!ids || !packed || !out) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_embed(ids, T, packed, K, N, g, out, err, static_cast<cudaStream_t>(stream)));
+}
+
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
   int st = check_shape(K, N, g);
   if (st != W4A16_OK) return st;

@@ -1,0 +1,71 @@
+// embed.cu -- gather of the quantized tied embedding: out[t][k] = W[k][ids[t]], fp16, bit-exact.
+//
+// The LM head's packed weight doubles as the embedding table: the head is tied to the
+// embedding (vllm-omni commit "cpu_int4: repack weights in n-blocks, to bound the load-time
+// peak": "embedding 131072 x 2048 ... tied, so it is also the head"; commit "Add cpu_int4 ...":
+// "the quantized tied embedding").  A token id n selects column n of W [K][N], and its
+// embedding row is that column dequantized: fp16((q[k][n] - z[k/g][n]) * s[k/g][n]) with the
+// same single rounding as the dequantized weight (dq.cuh).
+//
+// In the packed layout a column is one 64-byte row of each of its n-block's chunks, so a token
+// reads K/2 bytes of codes in 64-byte runs plus its scale and zero per group.  One CTA of 128
+// threads takes a token and 8 chunks (1024 k): thread i converts code word i % 16 (8 k) of
+// chunk i / 16 and stores 16 bytes of the output row, so a warp's stores are 512 contiguous
+// bytes.  An id outside [0, N) gives a row of zeros and records a device-side error.
+#include <cuda_runtime.h>
+
+#include "dq.cuh"
+#include "kernels.h"
+#include "layout.cuh"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kEmbedThreads = 128;
+constexpr int kChunksPerCta = kEmbedThreads / 16;
+
+__global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const int32_t *__restrict__ ids,
+                                                              const uint8_t *__restrict__ packed, int K, int N,
+                                                              int g, int KT, uint16_t *__restrict__ out, int *err) {
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * kChunksPerCta + threadIdx.x / 16;  // chunk (k-tile) of this thread
+  const int w = threadIdx.x % 16;                                // code word of the column row
+  const int k0 = c * kTileK + 8 * w;
+  const Header *h = reinterpret_cast<const Header *>(packed);
+  const bool hdr_ok = h->magic == kMagic && h->version == kLayoutVersion && h->K == K && h->N == N && h->g == g;
+  if (!hdr_ok) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, 1);
+    return;  // a mismatched buffer writes nothing
+  }
+  if (c >= KT || k0 >= K) return;
+  const int n = __ldg(ids + t);
+  uint4 o = make_uint4(0, 0, 0, 0);
+  if (n < 0 || n >= N) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, 4);
+  } else {
+    const int b = n / kBlockN, rr = n % kBlockN, p = meta_pos(rr);
+    const uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + c) * chunk_bytes(g);
+    const uint32_t word = __ldg(reinterpret_cast<const uint32_t *>(chunk + rr * kRowBytes) + w);
+    const uint8_t *meta = chunk + kCodeBytes + ((8 * w) / g) * kGroupMetaBytes;
+    const uint32_t s = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
+    const uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
+    uint32_t v[4];
+    word_to_qz(word, zero_bias((zw >> (4 * (p % 8))) & 0xFu), v);
+    const uint32_t s2 = s * 0x00010001u;
+    o = make_uint4(hmul2_u32(v[0], s2), hmul2_u32(v[1], s2), hmul2_u32(v[2], s2), hmul2_u32(v[3], s2));
+  }
+  *reinterpret_cast<uint4 *>(out + (size_t)t * K + k0) = o;
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                         int *err, cudaStream_t stream) {
+  const int KT = num_ktiles(K);
+  dim3 grid(T, (KT + kChunksPerCta - 1) / kChunksPerCta);
+  embed_kernel<<<grid, kEmbedThreads, 0, stream>>>(ids, static_cast<const uint8_t *>(packed), K, N, g, KT, out,
+                                                   err);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

@@ -31,6 +31,10 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K);
 // W4A16_SPLITK_AUTO or W4A16_SPLITK_GLOBAL (include/w4a16.h); returns a W4A16 status.
 int set_splitk_mode(int mode);
 
+// Tied-embedding gather: out[t][k] = fp16 W[k][ids[t]] for t < T (grid T x ceil(KT / 8)).
+cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                         int *err, cudaStream_t stream);
+
 // Device address of the library's per-device error word on the current device (null on failure).
 int *device_error_word();
 
