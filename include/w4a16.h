@@ -30,7 +30,12 @@
  *    nothing and keeps no pointer after the call returns.  Every call is asynchronous and
  *    ordered on `stream` (a cudaStream_t; NULL means the legacy default stream).  Apart from
  *    w4a16_last_device_error, no call synchronizes.
- *  - Shapes are int; K, N, g > 0.  Supported: g in {32, 64, 128}, K % g == 0, N % 8 == 0.
+ *  - Shapes are int; K, N > 0.  Supported group sizes: g in {32, 64, 128} with K % g == 0, or
+ *    one group over all of K (per-channel: g == K or g == -1, the group_size = -1 of section
+ *    "Limites y fallos", with K % 32 == 0; the scales and zeros then have one row).  N % 8 == 0.
+ *    The packed layout stores per-channel weights with g = the largest of 128, 64, 32 dividing
+ *    K, every group carrying the column's one scale and zero, so the weights are unchanged;
+ *    pass the same g (K or -1) to every call on that buffer.
  *    N need not be a multiple of 64 and K need not be a multiple of 128.
  *  - Device pointers must be 16-byte aligned.
  *  - Return value: W4A16_OK or a negative status (below).  No C++ exception crosses the ABI.
@@ -50,8 +55,8 @@ extern "C" {
 
 /* Status codes. */
 #define W4A16_OK 0
-#define W4A16_ERR_INVALID (-1)     /* null pointer, K/N/g <= 0, M < 0, bad n-range          */
-#define W4A16_ERR_UNSUPPORTED (-2) /* N % 8 != 0, K % g != 0, g not in {32, 64, 128}         */
+#define W4A16_ERR_INVALID (-1)     /* null pointer, K/N <= 0, g 0 or < -1, M < 0, bad n-range */
+#define W4A16_ERR_UNSUPPORTED (-2) /* N % 8 != 0, K % g != 0, g not 32/64/128/K/-1            */
 #define W4A16_ERR_MISALIGNED (-3)  /* a device pointer is not 16-byte aligned                */
 #define W4A16_ERR_WORKSPACE (-4)   /* workspace smaller than w4a16_workspace_bytes           */
 #define W4A16_ERR_CUDA (-5)        /* a CUDA call or kernel launch failed                    */

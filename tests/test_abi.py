@@ -119,3 +119,16 @@ def test_embed_host_validation(L):
     assert L.w4a16_embed(P, 4, P, 2048, 2048, 128, P4, NUL) == binding.ERR_MISALIGNED  # out
     assert L.w4a16_embed(ctypes.c_void_p(0x10002), 4, P, 2048, 2048, 128, P, NUL) == binding.ERR_MISALIGNED
     assert L.w4a16_embed(NUL, 0, NUL, 2048, 2048, 128, NUL, NUL) == binding.OK          # T = 0: no-op
+
+
+def test_per_channel_group_sizes(L):
+    """One group over all of K (g == K or g == -1) is stored with the largest of 128, 64, 32
+    dividing K; K % 32 != 0 is unsupported; other g values are rejected."""
+    assert L.w4a16_packed_bytes(2048, 3072, -1) == L.w4a16_packed_bytes(2048, 3072, 128)
+    assert L.w4a16_packed_bytes(2048, 3072, 2048) == L.w4a16_packed_bytes(2048, 3072, 128)
+    assert L.w4a16_packed_bytes(192, 136, 192) == L.w4a16_packed_bytes(192, 136, 64)
+    assert L.w4a16_packed_bytes(160, 80, -1) == L.w4a16_packed_bytes(160, 80, 32)
+    assert L.w4a16_packed_bytes(200, 80, -1) == 0                     # K % 32 != 0
+    assert L.w4a16_packed_bytes(2048, 3072, 256) == 0                 # neither 32/64/128 nor K
+    assert L.w4a16_gemm(P, P, 1, 3072, 2048, -2, P, NUL, 0, NUL) == binding.ERR_INVALID
+    assert L.w4a16_gemm(P, P, 1, 80, 200, -1, P, NUL, 0, NUL) == binding.ERR_UNSUPPORTED

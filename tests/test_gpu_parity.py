@@ -446,3 +446,28 @@ def test_embed_empty_is_noop():
     L = Layer(K, N, 128, seed=6)
     out = w4.embed(torch.empty(0, dtype=torch.int32, device=dev()), L.packed, K, N, 128)
     assert out.shape == (0, K)
+
+
+# ------------------------------------------------------------------ per-channel groups
+
+@pytest.mark.parametrize("K,N", [(2048, 3072), (192, 136), (160, 80)])
+@pytest.mark.parametrize("gpass", ["K", -1])
+def test_per_channel_groups(K, N, gpass):
+    """One group over all of K (the pages' group_size = -1): repacked from one row of scales and
+    zeros, the dequantized weights are bit-exact and the GEMM (decode and tensor-core paths)
+    meets the tolerance, against the oracle run with g = K."""
+    g = K if gpass == "K" else -1
+    L = Layer(K, N, K, seed=K + N)                      # qzeros [1][N/8], scales [1][N]
+    packed = w4.repack(L.d_qweight, L.d_qzeros, L.d_scales, K, N, g)
+    W = w4.dequant(packed, K, N, g).cpu().numpy().view(np.uint16)
+    assert np.array_equal(W, oracle.dequant_f16_bits(L.qweight, L.qzeros, L.scales_bits, K, N, K))
+    for M in (1, 24, 40, 300):
+        x = inputs.make_x(M, K, seed=M)
+        y = w4.gemm(torch.from_numpy(x).to(dev()), packed, M, N, K, g)
+        _, y16 = oracle.linear(x.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, K)
+        assert_close(y, y16)
+    ids = np.array([0, N - 1, 3, 3], np.int32)
+    e = w4.embed(torch.from_numpy(ids).to(dev()), packed, K, N, g).cpu().numpy().view(np.uint16)
+    ref, _ = oracle.embed_gather(L.qweight, L.qzeros, L.scales_bits, K, N, K, ids)
+    assert np.array_equal(e, ref)
+    assert w4.last_device_error() == 0

@@ -35,14 +35,25 @@ int *w4a16::device_error_word() {
   return g_err_ptr[dev];
 }
 
+// The group size the packed layout uses for a caller's g: g itself for 32, 64, 128 (K % g == 0);
+// for one group over all of K (g == K or g == -1, the pages' group_size = -1), the largest of
+// 128, 64, 32 that divides K, every layout group then carrying the column's one scale and zero.
+// 0 when unsupported.
+int w4a16::layout_group(int K, int g) {
+  if (K <= 0) return 0;
+  if (g == 32 || g == 64 || g == 128) return K % g == 0 ? g : 0;
+  if (g == K || g == -1)
+    return K % 128 == 0 ? 128 : K % 64 == 0 ? 64 : K % 32 == 0 ? 32 : 0;
+  return 0;
+}
+
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int K, int N, int g) {
-  if (K <= 0 || N <= 0 || g <= 0) return W4A16_ERR_INVALID;
-  if (g != 32 && g != 64 && g != 128) return W4A16_ERR_UNSUPPORTED;
-  if (N % 8 != 0 || K % g != 0) return W4A16_ERR_UNSUPPORTED;
+  if (K <= 0 || N <= 0 || g == 0 || g < -1) return W4A16_ERR_INVALID;
+  if (N % 8 != 0 || layout_group(K, g) == 0) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
 }
 
@@ -60,7 +71,7 @@ extern "C" {
 
 size_t w4a16_packed_bytes(int K, int N, int g) {
   if (check_shape(K, N, g) != W4A16_OK) return 0;
-  return (size_t)kHeaderBytes + (size_t)num_nblocks(N) * num_ktiles(K) * chunk_bytes(g);
+  return (size_t)kHeaderBytes + (size_t)num_nblocks(N) * num_ktiles(K) * chunk_bytes(layout_group(K, g));
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
@@ -82,8 +93,10 @@ int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight, const int32
   if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(qweight_c) & 3u) ||
       (reinterpret_cast<uintptr_t>(qzeros_c) & 3u) || (reinterpret_cast<uintptr_t>(scales_c) & 1u))
     return W4A16_ERR_MISALIGNED;
+  const int gl = layout_group(K, g);
+  const int gsrc = (g == -1) ? K : g;  // rows of K per row of the source scales and zeros
   return map_launch(launch_repack(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales,
-                                  K, N, g, n0, n1, packed, static_cast<cudaStream_t>(stream)));
+                                  K, N, gl, gsrc, n0, n1, packed, static_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_repack(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K,
@@ -111,8 +124,9 @@ int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, g, y, err, s));
-  return map_launch(launch_gemm_tc(x, packed, M, N, K, g, y, err, workspace, s));
+  const int gl = layout_group(K, g);
+  if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, gl, y, err, s));
+  return map_launch(launch_gemm_tc(x, packed, M, N, K, gl, y, err, workspace, s));
 }
 
 int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
@@ -125,7 +139,7 @@ int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int
   if (!aligned16(packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return W4A16_ERR_MISALIGNED;
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
-  return map_launch(launch_embed(ids, T, packed, K, N, g, out, err, static_cast<cudaStream_t>(stream)));
+  return map_launch(launch_embed(ids, T, packed, K, N, layout_group(K, g), out, err, static_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
@@ -135,7 +149,7 @@ int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *st
   if (!aligned16(packed) || !aligned16(W)) return W4A16_ERR_MISALIGNED;
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
-  return map_launch(launch_dequant(packed, K, N, g, W, err, static_cast<cudaStream_t>(stream)));
+  return map_launch(launch_dequant(packed, K, N, layout_group(K, g), W, err, static_cast<cudaStream_t>(stream)));
 }
 
 const char *w4a16_status_string(int status) {

@@ -9,10 +9,12 @@
 namespace w4a16 {
 
 // Repack columns [n0, n1) of AWQ tensors (slices starting at column n0, row strides in
-// elements) into their n-blocks of `packed`, and write the header.
+// elements) into their n-blocks of `packed`, and write the header.  g is the layout's group
+// size (32, 64, 128); the source tensors' scales and zeros have one row per gsrc rows of K
+// (gsrc == g, or gsrc == K for one group over all of K).
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
-                          const uint16_t *scales, int64_t lds, int K, int N, int g, int n0, int n1,
-                          void *packed, cudaStream_t stream);
+                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
+                          int n1, void *packed, cudaStream_t stream);
 
 // packed -> fp16 W[K][N].
 cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W, int *err,
@@ -34,6 +36,10 @@ int set_splitk_mode(int mode);
 // Tied-embedding gather: out[t][k] = fp16 W[k][ids[t]] for t < T (grid T x ceil(KT / 8)).
 cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
                          int *err, cudaStream_t stream);
+
+// The packed layout's group size for a caller's g (32, 64 or 128; or one group over all of K,
+// g == K or g == -1, stored as the largest of 128, 64, 32 dividing K); 0 when unsupported.
+int layout_group(int K, int g);
 
 // Device address of the library's per-device error word on the current device (null on failure).
 int *device_error_word();

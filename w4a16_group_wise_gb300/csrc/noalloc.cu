@@ -63,8 +63,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 #pragma GCC visibility push(default)
 extern "C" int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                                   void *stream) {
-  if (M < 0 || K <= 0 || N <= 0 || g <= 0) return W4A16_ERR_INVALID;
-  if ((g != 32 && g != 64 && g != 128) || N % 8 != 0 || K % g != 0) return W4A16_ERR_UNSUPPORTED;
+  if (M < 0 || K <= 0 || N <= 0 || g == 0 || g < -1) return W4A16_ERR_INVALID;
+  if (N % 8 != 0 || layout_group(K, g) == 0) return W4A16_ERR_UNSUPPORTED;
   if (M == 0) return W4A16_OK;
   if (!x || !packed || !y) return W4A16_ERR_INVALID;
   if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
@@ -74,8 +74,9 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, 
   int *err = device_error_word();
   if (!scratch || !err) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (M <= kDecodeMaxM) ? launch_gemv(x, packed, M, N, K, g, y, err, s)
-                                     : launch_gemm_tc(x, packed, M, N, K, g, y, err, scratch, s);
+  const int gl = layout_group(K, g);
+  cudaError_t e = (M <= kDecodeMaxM) ? launch_gemv(x, packed, M, N, K, gl, y, err, s)
+                                     : launch_gemm_tc(x, packed, M, N, K, gl, y, err, scratch, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;

@@ -24,7 +24,7 @@ __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 *
 
 __global__ void __launch_bounds__(256) repack_kernel(
     const int32_t *__restrict__ qweight, int64_t ldq, const int32_t *__restrict__ qzeros,
-    int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int n0,
+    int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
     int b0, int KT, uint8_t *__restrict__ packed) {
   const int b = b0 + blockIdx.x;  // n-block
   const int t = blockIdx.y;       // k-tile
@@ -70,26 +70,30 @@ __global__ void __launch_bounds__(256) repack_kernel(
     codes[i] = out;
   }
 
-  // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.
+  // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
+  // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
+  // source tensors (gsrc == g, or gsrc == K for one group over all of K).
   const int gpc = kTileK / g;  // groups per chunk
   const int G = K / g;
   for (int i = threadIdx.x; i < gpc * kBlockN; i += blockDim.x) {
     int l = i / kBlockN, p = i % kBlockN;
     int grp = t * gpc + l, n = b * kBlockN + meta_row(p);
+    int sg = (grp * g) / gsrc;
     uint16_t s = 0;
-    if (grp < G && n < N) s = scales[(int64_t)grp * lds + (n - n0)];
+    if (grp < G && n < N) s = scales[(int64_t)sg * lds + (n - n0)];
     reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes)[p] = s;
   }
   for (int i = threadIdx.x; i < gpc * 8; i += blockDim.x) {
     int l = i / 8, wi = i % 8;
     int grp = t * gpc + l;
+    int sg = (grp * g) / gsrc;
     uint32_t out = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       int n = b * kBlockN + meta_row(8 * wi + j);
       uint32_t z = 0;
       if (grp < G && n < N) {
-        uint32_t zw = (uint32_t)qzeros[(int64_t)grp * ldz + (n - n0) / 8];
+        uint32_t zw = (uint32_t)qzeros[(int64_t)sg * ldz + (n - n0) / 8];
         z = (zw >> (4 * awq_slot_of_col(n & 7))) & 0xFu;
       }
       out |= z << (4 * j);
@@ -101,13 +105,13 @@ __global__ void __launch_bounds__(256) repack_kernel(
 }  // namespace
 
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
-                          const uint16_t *scales, int64_t lds, int K, int N, int g, int n0, int n1,
-                          void *packed, cudaStream_t stream) {
+                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
+                          int n1, void *packed, cudaStream_t stream) {
   int b0 = n0 / kBlockN;
   int b1 = (n1 + kBlockN - 1) / kBlockN;
   int KT = num_ktiles(K);
   dim3 grid(b1 - b0, KT);
-  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, n0, b0,
+  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, n0, b0,
                                           KT, static_cast<uint8_t *>(packed));
   return cudaGetLastError();
 }
