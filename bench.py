@@ -274,7 +274,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- prefill M=512 (secondary): TFLOP/s of the three shapes
     prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
-    embed = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
+    embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
 
     gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
     traffic = None
@@ -294,6 +294,7 @@ def run_ours(args, rank, world, local_rank):
         "per_shape": per_shape,
         "prefill": prefill,
         "embed": embed,
+        "awq_to_standard": convert,
         "e2e": e2e,
         "gpu_launches": len(launches) * args.steps,
         "clocks": clk.summary(),
@@ -306,9 +307,24 @@ def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
     (K=2048, N=131072), GB/s of algorithmic bytes (codes, scale and zero per group, id, fp16 row)."""
     K, N = inputs.SHAPES["lm_head"]
     h = inputs.make_weights(K, N, G, seed=31)
-    packed = w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
-                       torch.from_numpy(h["scales"]).to(dev), K, N, G, stream=stream)
+    qw, qz = torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev)
+    packed = w4.repack(qw, qz, torch.from_numpy(h["scales"]).to(dev), K, N, G, stream=stream)
     del h
+    # the one-time AWQ -> standard conversion of the same tensors (bytes read + written)
+    with torch.cuda.stream(stream):
+        w4.awq_to_standard(qw, qz, K, N, G, stream=stream)
+
+    def conv():
+        with torch.cuda.stream(stream):
+            w4.awq_to_standard(qw, qz, K, N, G, stream=stream)
+    ms_conv = timed(conv, 10) / 10
+    conv_bytes = 2 * (qw.numel() + qz.numel()) * 4
+    conv_gbs = conv_bytes / (ms_conv * 1e-3) / 1e9
+    convert = {"metric": "AWQ -> standard repacking GB/s (%dx%d LM head tensors, read + written)" % (K, N),
+               "value": round(conv_gbs, 1), "unit": "GB/s", "us_per_call": round(ms_conv * 1e3, 1),
+               "roofline": {"bound": "hbm", "achieved": round(conv_gbs, 1), "peak": hbm, "unit": "GB/s",
+                            "frac": round(conv_gbs / hbm, 4), "peak_source": peak_src}}
+    del qw, qz
     ids = torch.from_numpy(np.random.default_rng(32).integers(0, N, T).astype(np.int32)).to(dev)
     out = torch.empty((T, K), dtype=torch.float16, device=dev)
     reps_in_graph = 10
@@ -332,7 +348,7 @@ def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
     return {"metric": "tied-embedding gather GB/s (%d token rows of the %dx%d LM head, g=%d)" % (T, K, N, G),
             "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "peak_source": peak_src}}
+                         "frac": round(gbs / hbm, 4), "peak_source": peak_src}}, convert
 
 
 def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src):

@@ -150,6 +150,17 @@ int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *st
 int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
                 void *stream);
 
+/* AWQ packing -> the GPTQ-style "standard" packing ("Carga de capas cuantizadas: AWQ / GPTQ /
+ * Marlin / fp8", section "Motivacion de diseno": AWQ packs along the output dimension in a
+ * non-standard order, the standard format along the input dimension in plain order), integer
+ * exact.  In: qweight_awq int32 [K][N/8], qzeros_awq int32 [K/g][N/8] (one row per-channel).
+ * Out (fully written): qweight_std int32 [K/8][N], nibble j of word (r, n) = q[8r + j][n];
+ * qzeros_std int32 [K/g][N/8], nibble j of word (G, c) = z[G][8c + j].  The scales are shared
+ * by both formats.  qweight_std 16-byte aligned, the other pointers 4-byte aligned; the outputs
+ * must not overlap the inputs. */
+int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N, int g,
+                          int32_t *qweight_std, int32_t *qzeros_std, void *stream);
+
 /* Size of the scratch array built into the library for w4a16_gemm_noalloc (24 MiB): every GPU
  * that loads the library keeps this much device memory for the life of the process. */
 #define W4A16_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -132,3 +132,14 @@ def test_per_channel_group_sizes(L):
     assert L.w4a16_packed_bytes(2048, 3072, 256) == 0                 # neither 32/64/128 nor K
     assert L.w4a16_gemm(P, P, 1, 3072, 2048, -2, P, NUL, 0, NUL) == binding.ERR_INVALID
     assert L.w4a16_gemm(P, P, 1, 80, 200, -1, P, NUL, 0, NUL) == binding.ERR_UNSUPPORTED
+
+
+def test_awq_to_standard_host_validation(L):
+    # every case is rejected before any launch (the pointers are never dereferenced)
+    P2 = ctypes.c_void_p(0x10002)
+    assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 100, P, P, NUL) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_awq_to_standard(NUL, P, 2048, 3072, 128, P, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 128, P, NUL, NUL) == binding.ERR_INVALID
+    assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 128, P2, P, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_awq_to_standard(P, P2, 2048, 3072, 128, P, P, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 128, ctypes.c_void_p(0x10004), P, NUL) == binding.ERR_MISALIGNED

@@ -471,3 +471,16 @@ def test_per_channel_groups(K, N, gpass):
     ref, _ = oracle.embed_gather(L.qweight, L.qzeros, L.scales_bits, K, N, K, ids)
     assert np.array_equal(e, ref)
     assert w4.last_device_error() == 0
+
+
+# ------------------------------------------------------------------ AWQ -> standard packing
+
+@pytest.mark.parametrize("K,N,g", [(2048, 3072, 128), (6656, 80, 32), (192, 136, 192), (160, 80, -1)])
+def test_awq_to_standard_bit_exact(K, N, g):
+    """The GPU conversion to the GPTQ-style standard packing equals the oracle's word for word
+    (N = 80 tail, per-channel groups passed as g = K and as g = -1)."""
+    L = Layer(K, N, K if g == -1 else g, seed=K + N + 1)
+    qs, zs = w4.awq_to_standard(L.d_qweight, L.d_qzeros, K, N, g)
+    rqs, rzs = oracle.awq_to_standard(L.qweight, L.qzeros, K, N, K if g == -1 else g)
+    assert np.array_equal(qs.cpu().numpy(), rqs)
+    assert np.array_equal(zs.cpu().numpy(), rzs)

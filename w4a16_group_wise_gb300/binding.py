@@ -40,6 +40,7 @@ SIGNATURES = {
     "w4a16_gemm_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
     "w4a16_set_option": ([_I, _I], _I),
     "w4a16_embed": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
+    "w4a16_awq_to_standard": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
 }
 
 _lib = None
@@ -193,6 +194,17 @@ def embed(ids, packed, K, N, g, out=None, stream=None):
         out = torch.empty((T, K), dtype=torch.float16, device=ids.device)
     _check("w4a16_embed", lib().w4a16_embed(_ptr(ids), T, _ptr(packed), K, N, g, _ptr(out), _stream(stream)))
     return out
+
+
+def awq_to_standard(qweight, qzeros, K, N, g, stream=None):
+    """AWQ int32 tensors -> (qweight_std int32 [K/8, N], qzeros_std int32 [K/g, N/8])."""
+    _dev(qweight, torch.int32, "qweight")
+    _dev(qzeros, torch.int32, "qzeros")
+    qs = torch.empty((K // 8, N), dtype=torch.int32, device=qweight.device)
+    zs = torch.empty_like(qzeros)
+    _check("w4a16_awq_to_standard", lib().w4a16_awq_to_standard(_ptr(qweight), _ptr(qzeros), K, N, g, _ptr(qs),
+                                                                 _ptr(zs), _stream(stream)))
+    return qs, zs
 
 
 def last_device_error(stream=None):

@@ -142,6 +142,19 @@ int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int
   return map_launch(launch_embed(ids, T, packed, K, N, layout_group(K, g), out, err, static_cast<cudaStream_t>(stream)));
 }
 
+int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N, int g,
+                          int32_t *qweight_std, int32_t *qzeros_std, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!qweight_awq || !qzeros_awq || !qweight_std || !qzeros_std) return W4A16_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(qweight_awq) & 3u) || (reinterpret_cast<uintptr_t>(qzeros_awq) & 3u) ||
+      !aligned16(qweight_std) || (reinterpret_cast<uintptr_t>(qzeros_std) & 3u))
+    return W4A16_ERR_MISALIGNED;
+  const int zero_rows = (g == -1 || g == K) ? 1 : K / g;
+  return map_launch(launch_awq_to_standard(qweight_awq, qzeros_awq, K, N, zero_rows, qweight_std, qzeros_std,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
   int st = check_shape(K, N, g);
   if (st != W4A16_OK) return st;

@@ -1,0 +1,70 @@
+// convert.cu -- AWQ packing -> the GPTQ-style "standard" packing, integer-exact.
+//
+// vLLM walkthrough "Carga de capas cuantizadas: AWQ / GPTQ / Marlin / fp8", section
+// "Motivacion de diseno": AWQ packs its codes along the output dimension in a non-standard
+// order, where the standard (GPTQ-style) checkpoints pack along the input dimension in plain
+// order.  Out:
+//   qweight_std int32 [K/8][N]:   nibble slot j (bits 4j..4j+3) of word (r, n) = q[8r + j][n];
+//   qzeros_std  int32 [K/g][N/8]: nibble slot j of word (G, c) = z[G][8c + j];
+// the scales are the same tensor in both formats.  In AWQ words column 8c + o sits in slot
+// {0,4,1,5,2,6,3,7}[o] (the inverse of the slot order {0,2,4,6,1,3,5,7}).
+//
+// qweight: one thread per (row octet, AWQ word column) reads the 8 words of rows 8r..8r+7
+// (consecutive threads read consecutive words) and writes the 8 output words of its column
+// octet as 32 contiguous bytes.  qzeros: one thread per word permutes its nibbles.
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace w4a16 {
+namespace {
+
+__device__ __forceinline__ int awq_slot(int o) { return (o & 1) ? 4 + (o >> 1) : (o >> 1); }
+
+__global__ void __launch_bounds__(256) awq_to_standard_q_kernel(const int32_t *__restrict__ qa, int K, int N,
+                                                                int32_t *__restrict__ qs) {
+  const int C = N / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row octet r, word column c)
+  if (i >= (int64_t)(K / 8) * C) return;
+  const int r = (int)(i / C), c = (int)(i % C);
+  uint32_t in[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) in[j] = (uint32_t)__ldg(qa + (int64_t)(8 * r + j) * C + c);
+  uint32_t out[8];
+#pragma unroll
+  for (int o = 0; o < 8; ++o) {  // column 8c + o: its nibble of rows 8r .. 8r+7
+    const int sh = 4 * awq_slot(o);
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w |= ((in[j] >> sh) & 0xFu) << (4 * j);
+    out[o] = w;
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(qs + (int64_t)r * N + 8 * c);  // 32 contiguous bytes
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+__global__ void __launch_bounds__(256) awq_to_standard_z_kernel(const int32_t *__restrict__ za, int64_t words,
+                                                                int32_t *__restrict__ zs) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= words) return;
+  const uint32_t src = (uint32_t)__ldg(za + i);
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w |= ((src >> (4 * awq_slot(j))) & 0xFu) << (4 * j);
+  zs[i] = (int32_t)w;
+}
+
+}  // namespace
+
+cudaError_t launch_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N,
+                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std,
+                                   cudaStream_t stream) {
+  const int64_t qthreads = (int64_t)(K / 8) * (N / 8), zwords = (int64_t)zero_rows * (N / 8);
+  awq_to_standard_q_kernel<<<(unsigned)((qthreads + 255) / 256), 256, 0, stream>>>(qweight_awq, K, N, qweight_std);
+  if (zwords > 0)
+    awq_to_standard_z_kernel<<<(unsigned)((zwords + 255) / 256), 256, 0, stream>>>(qzeros_awq, zwords, qzeros_std);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

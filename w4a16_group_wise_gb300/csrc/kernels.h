@@ -37,6 +37,12 @@ int set_splitk_mode(int mode);
 cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
                          int *err, cudaStream_t stream);
 
+// AWQ -> GPTQ-style standard packing: qweight [K/8][N] packed along K in plain order, qzeros
+// [zero_rows][N/8] in plain order along N.
+cudaError_t launch_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N,
+                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std,
+                                   cudaStream_t stream);
+
 // The packed layout's group size for a caller's g (32, 64 or 128; or one group over all of K,
 // g == K or g == -1, stored as the largest of 128, 64, 32 dividing K); 0 when unsupported.
 int layout_group(int K, int g);
