@@ -51,6 +51,12 @@ def lib():
             "oracle_int4pack_cpu": ([P, I, I, P], None),
             "oracle_int4unpack_cpu": ([P, I, I, P], None),
             "oracle_embed_gather": ([P, P, P, I, I, I, P, I, P], I),
+            "oracle_bf16_to_double": ([ctypes.c_uint16], ctypes.c_double),
+            "oracle_double_to_bf16": ([ctypes.c_double], ctypes.c_uint16),
+            "oracle_double_to_bf16_array": ([P, I64, P], None),
+            "oracle_dequant_awq_bf16_f64": ([P, P, P, I, I, I, P], I),
+            "oracle_dequant_awq_bf16": ([P, P, P, I, I, I, P], I),
+            "oracle_linear_bf16": ([P, I, I, P, P, P, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -225,3 +231,38 @@ def int4unpack_cpu(packed, K, N):
     q = np.empty((K, N), np.uint8)
     lib().oracle_int4unpack_cpu(_p(packed), K, N, _p(q))
     return q
+
+
+# ------------------------------------------------------------------ the bf16 layer
+
+def bf16_bits_to_double(b):
+    b = _c(b, np.uint16)
+    f = np.vectorize(lib().oracle_bf16_to_double, otypes=[np.float64])
+    return f(b) if b.size else np.empty(b.shape, np.float64)
+
+
+def double_to_bf16_bits(v):
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().oracle_double_to_bf16_array(_p(v), v.size, _p(out))
+    return out
+
+
+def dequant_bf16_bits(qweight, qzeros, scales_bits, K, N, g):
+    qw, qz, s = _c(qweight, np.int32), _c(qzeros, np.int32), _c(scales_bits, np.uint16)
+    W = np.empty((K, N), np.uint16)
+    if lib().oracle_dequant_awq_bf16(_p(qw), _p(qz), _p(s), K, N, g, _p(W)):
+        raise MemoryError("oracle_dequant_awq_bf16")
+    return W
+
+
+def linear_bf16(x_bits, qweight, qzeros, scales_bits, K, N, g):
+    """bf16 layer: returns (y in double, y rounded to bfloat16 bits)."""
+    x = _c(x_bits, np.uint16)
+    M = x.shape[0]
+    qw, qz, s = _c(qweight, np.int32), _c(qzeros, np.int32), _c(scales_bits, np.uint16)
+    y64 = np.empty((M, N), np.float64)
+    yb = np.empty((M, N), np.uint16)
+    if lib().oracle_linear_bf16(_p(x), M, K, _p(qw), _p(qz), _p(s), N, g, _p(y64), _p(yb)):
+        raise MemoryError("oracle_linear_bf16")
+    return y64, yb

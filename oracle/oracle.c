@@ -107,6 +107,56 @@ void oracle_half_to_double_array(const uint16_t *in, int64_t n, double *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_half_to_double(in[i]);
 }
 
+/* ---------------------------------------------------------------- bfloat16 -------------- */
+/* The bf16 variant of the layer (activations, scales and output in bfloat16: the CPU path of
+ * vllm-omni commit "Add cpu_int4 ..." runs in bf16).  bfloat16: 1 sign bit, 8 exponent bits
+ * (bias 127), 7 fraction bits, gradual underflow. */
+
+/* Exact value of a bfloat16 bit pattern. */
+double oracle_bf16_to_double(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);                /* subnormal: f * 2^-133 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134);     /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest bfloat16, ties to even, with gradual underflow and overflow to
+ * infinity (same construction as the binary16 rounding above, with bfloat16's parameters). */
+uint16_t oracle_double_to_bf16(double v) {
+    if (isnan(v)) return 0x7fc0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7f80;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;                                 /* a in [2^E, 2^(E+1)) */
+    if (E > 127) return sign | 0x7f80;
+    int qexp = (E >= -126) ? (E - 7) : -133;        /* spacing of bfloat16 values near a */
+    double scaled = ldexp(a, -qexp);
+    double S = floor(scaled);
+    double rem = scaled - S;
+    if (rem > 0.5 || (rem == 0.5 && fmod(S, 2.0) != 0.0)) S += 1.0;
+    if (E < -126) return sign | (uint16_t)S;        /* S == 128 is the smallest normal, 0x0080 */
+    if (S >= 256.0) {
+        S = 128.0;
+        E += 1;
+        if (E > 127) return sign | 0x7f80;
+    }
+    return sign | (uint16_t)(((E + 127) << 7) | ((int)S - 128));
+}
+
+void oracle_double_to_bf16_array(const double *in, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_double_to_bf16(in[i]);
+}
+
 /* ---------------------------------------------------------------- AWQ packing ----------- */
 
 /* Unpack AWQ-packed codes: packed int32 [rows][N/8] -> codes uint8 [rows][N].
@@ -135,18 +185,26 @@ void oracle_awq_pack(const uint8_t *codes, int rows, int N, int32_t *packed) {
 
 /* ---------------------------------------------------------------- dequantization -------- */
 
-/* W[k][n] = (q[k][n] - z[k/g][n]) * s[k/g][n], exact in double. */
-void oracle_dequant_codes_f64(const uint8_t *q, const uint8_t *z, const uint16_t *s,
-                              int K, int N, int g, double *W) {
+typedef double (*decode16_fn)(uint16_t);
+
+/* W[k][n] = (q[k][n] - z[k/g][n]) * s[k/g][n], exact in double, s decoded by `dec`. */
+static void dequant_codes_dec(const uint8_t *q, const uint8_t *z, const uint16_t *s,
+                              int K, int N, int g, decode16_fn dec, double *W) {
     for (int k = 0; k < K; ++k) {
         int G = k / g;
         for (int n = 0; n < N; ++n) {
             double qv = (double)q[(int64_t)k * N + n];
             double zv = (double)z[(int64_t)G * N + n];
-            double sv = oracle_half_to_double(s[(int64_t)G * N + n]);
+            double sv = dec(s[(int64_t)G * N + n]);
             W[(int64_t)k * N + n] = (qv - zv) * sv;
         }
     }
+}
+
+/* W[k][n] = (q[k][n] - z[k/g][n]) * s[k/g][n], exact in double (fp16 scales). */
+void oracle_dequant_codes_f64(const uint8_t *q, const uint8_t *z, const uint16_t *s,
+                              int K, int N, int g, double *W) {
+    dequant_codes_dec(q, z, s, K, N, g, oracle_half_to_double, W);
 }
 
 /* Dequantize straight from the AWQ tensors (qweight [K][N/8], qzeros [K/g][N/8],
@@ -354,4 +412,66 @@ void oracle_int4unpack_cpu(const uint8_t *packed, int K, int N, uint8_t *q) {
             uint8_t byte = packed[((int64_t)b * K + k) * 32 + (d % 32)];
             q[(int64_t)k * N + n] = d < 32 ? (byte & 0xF) : (byte >> 4);
         }
+}
+
+
+/* ---------------------------------------------------------------- the bf16 layer -------- */
+
+/* As oracle_dequant_awq_f64 with bfloat16 scales. */
+int oracle_dequant_awq_bf16_f64(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                                int K, int N, int g, double *W) {
+    int groups = K / g;
+    uint8_t *q = (uint8_t *)malloc((size_t)K * N);
+    uint8_t *z = (uint8_t *)malloc((size_t)groups * N);
+    if (!q || !z) { free(q); free(z); return -1; }
+    oracle_awq_unpack(qweight, K, N, q);
+    oracle_awq_unpack(qzeros, groups, N, z);
+    dequant_codes_dec(q, z, scales, K, N, g, oracle_bf16_to_double, W);
+    free(q);
+    free(z);
+    return 0;
+}
+
+/* The bfloat16 weight: one round-to-nearest-even of the exact product. */
+int oracle_dequant_awq_bf16(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                            int K, int N, int g, uint16_t *Wb) {
+    int64_t n = (int64_t)K * N;
+    double *W = (double *)malloc((size_t)n * sizeof(double));
+    if (!W) return -1;
+    if (oracle_dequant_awq_bf16_f64(qweight, qzeros, scales, K, N, g, W)) { free(W); return -1; }
+    oracle_double_to_bf16_array(W, n, Wb);
+    free(W);
+    return 0;
+}
+
+/* The bf16 layer: x bfloat16 [M][K], scales bfloat16; y64 = x * W in double (k summed in
+ * increasing order), yb = its bfloat16 rounding (either output may be NULL).  Returns 0, or -1
+ * if memory ran out. */
+int oracle_linear_bf16(const uint16_t *x, int M, int K, const int32_t *qweight, const int32_t *qzeros,
+                       const uint16_t *scales, int N, int g, double *y64, uint16_t *yb) {
+    double *W = (double *)malloc((size_t)K * N * sizeof(double));
+    double *y = y64 ? y64 : (double *)malloc((size_t)M * N * sizeof(double) + 1);
+    if (!W || !y) { free(W); if (!y64) free(y); return -1; }
+    if (oracle_dequant_awq_bf16_f64(qweight, qzeros, scales, K, N, g, W)) {
+        free(W); if (!y64) free(y); return -1;
+    }
+    const int NB = 256;
+    int nblocks = (N + NB - 1) / NB;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < nblocks; ++b) {
+        int n0 = b * NB, n1 = n0 + NB < N ? n0 + NB : N;
+        for (int m = 0; m < M; ++m) {
+            double *yr = y + (int64_t)m * N;
+            for (int n = n0; n < n1; ++n) yr[n] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double xv = oracle_bf16_to_double(x[(int64_t)m * K + k]);
+                const double *Wr = W + (int64_t)k * N;
+                for (int n = n0; n < n1; ++n) yr[n] += xv * Wr[n];
+            }
+        }
+    }
+    if (yb) oracle_double_to_bf16_array(y, (int64_t)M * N, yb);
+    free(W);
+    if (!y64) free(y);
+    return 0;
 }

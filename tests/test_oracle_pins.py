@@ -446,3 +446,84 @@ def test_embed_gather_matches_numpy_rounding():
             assert np.array_equal(out[t], exact.astype(np.float16).view(np.uint16)), t
         else:
             assert not out[t].any()
+
+
+# ------------------------------------------------------------------ bfloat16
+
+def _bf16_widen_np(bits):
+    """bfloat16 -> float64 by numpy alone: the pattern is the top half of a binary32."""
+    with np.errstate(invalid="ignore"):                 # NaN patterns widen to NaN
+        return (np.asarray(bits, np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+_ALL_BF16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+_FIN_BF16 = _ALL_BF16[np.isfinite(_bf16_widen_np(_ALL_BF16))]
+_FIN_VALS = _bf16_widen_np(_FIN_BF16)
+_ORDER = np.lexsort((_FIN_BF16, _FIN_VALS))          # by value; +0 before -0 sorts by pattern
+
+
+def _nearest_bf16_np(v):
+    """Brute-force round-to-nearest-even into bfloat16 over the sorted finite values."""
+    vals, pats = _FIN_VALS[_ORDER], _FIN_BF16[_ORDER]
+    v = np.asarray(v, np.float64)
+    i = np.clip(np.searchsorted(vals, v), 1, len(vals) - 1)
+    lo, hi = vals[i - 1], vals[i]
+    plo, phi = pats[i - 1], pats[i]
+    dlo, dhi = v - lo, hi - v
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (phi % 2 == 0))
+    return np.where(pick_hi, phi, plo).astype(np.uint16)
+
+
+def test_bf16_widening_is_exact_for_every_pattern():
+    got = oracle.bf16_bits_to_double(_ALL_BF16)
+    want = _bf16_widen_np(_ALL_BF16)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_bf16_rounding_nearest_even_and_round_trip():
+    # every finite pattern survives a round trip (the sign of zero included)
+    assert np.array_equal(oracle.double_to_bf16_bits(_bf16_widen_np(_FIN_BF16)), _FIN_BF16)
+    # midpoints between neighbours of one sign round to the even pattern
+    pos = np.sort(_FIN_VALS[_FIN_VALS > 0])
+    mids = (pos[:-1] + pos[1:]) / 2
+    want = _nearest_bf16_np(mids)
+    assert np.all(want % 2 == 0)
+    assert np.array_equal(oracle.double_to_bf16_bits(mids), want)
+    # random magnitudes across the whole normal and subnormal range, both signs
+    rng = np.random.default_rng(11)
+    v = rng.choice([-1, 1], 20000) * np.exp2(rng.uniform(-134, 127, 20000))
+    assert np.array_equal(oracle.double_to_bf16_bits(v), _nearest_bf16_np(v))
+
+
+def test_bf16_dequant_is_one_rounding_of_the_exact_product():
+    K, N, g = 256, 64, 64
+    rng = np.random.default_rng(12)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, (K // g, N)).astype(np.uint8)
+    sb = _nearest_bf16_np(rng.uniform(1e-3, 0.05, (K // g, N)))
+    got = oracle.dequant_bf16_bits(_pack_awq(q), _pack_awq(z), sb, K, N, g)
+    grp = np.arange(K) // g
+    exact = (q.astype(np.float64) - z[grp]) * _bf16_widen_np(sb)[grp]
+    assert np.array_equal(got, _nearest_bf16_np(exact))
+
+
+def test_bf16_linear_matches_numpy_and_is_exact_on_exact_sums():
+    K, N, g = 256, 48, 128
+    rng = np.random.default_rng(13)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, (K // g, N)).astype(np.uint8)
+    sb = _nearest_bf16_np(rng.uniform(1e-3, 0.05, (K // g, N)))
+    xb = _nearest_bf16_np(rng.standard_normal((3, K)))
+    grp = np.arange(K) // g
+    W = (q.astype(np.float64) - z[grp]) * _bf16_widen_np(sb)[grp]
+    y64, yb = oracle.linear_bf16(xb, _pack_awq(q), _pack_awq(z), sb, K, N, g)
+    ref = _bf16_widen_np(xb) @ W
+    assert np.allclose(y64, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(yb, _nearest_bf16_np(y64))
+    # x in {-2..2}, scales 2^-8: every partial sum is exact, so y is the integer product
+    xi = rng.integers(-2, 3, (2, K)).astype(np.float64)
+    s8 = np.full((K // g, N), 0x3B80, np.uint16)                        # bf16 2^-8
+    y64, _ = oracle.linear_bf16(_nearest_bf16_np(xi), _pack_awq(q), _pack_awq(z), s8, K, N, g)
+    assert np.array_equal(y64, (xi @ (q.astype(np.float64) - z[grp])) / 256.0)
