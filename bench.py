@@ -275,6 +275,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- prefill M=512 (secondary): TFLOP/s of the three shapes
     prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
     embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
+    bf16_layer = run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank)
 
     gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
     traffic = None
@@ -295,6 +296,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill": prefill,
         "embed": embed,
         "awq_to_standard": convert,
+        "bf16_layer": bf16_layer,
         "e2e": e2e,
         "gpu_launches": len(launches) * args.steps,
         "clocks": clk.summary(),
@@ -351,13 +353,21 @@ def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
                          "frac": round(gbs / hbm, 4), "peak_source": peak_src}}, convert
 
 
-def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src):
+def _x_on_device(torch, dev, M, K, seed, dtype):
+    """Seeded activations [M, K] on the device, fp16 or (dtype "bf16") bf16."""
+    x = inputs.make_x(M, K, seed=seed, dtype=dtype)
+    if dtype == "bf16":
+        return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(x).to(dev)
+
+
+def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src, dtype="f16"):
     M = 512
     out = {}
     tot_flops, tot_ms = 0.0, 0.0
     for si, (name, K, N) in enumerate(DECODE_SHAPES):
-        x = torch.from_numpy(inputs.make_x(M, K, seed=77)).to(dev)
-        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        x = _x_on_device(torch, dev, M, K, 77, dtype)
+        y = torch.empty((M, N), dtype=x.dtype, device=dev)
         ws = torch.zeros(max(1, w4.workspace_bytes(M, N, K, G)), dtype=torch.uint8, device=dev)
         sel = [lin[si][3] for lin in layers]
         g2 = torch.cuda.CUDAGraph()
@@ -382,11 +392,61 @@ def run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, pea
         tot_flops += fl
         tot_ms += ms
     tf = tot_flops / (tot_ms * 1e-3) / 1e12
-    out["all"] = {"metric": "TFLOP/s at M=512 (q_k_v, gate_up, down; fp16 x fp16 -> fp32)",
+    ops = "bf16 x bf16" if dtype == "bf16" else "fp16 x fp16"
+    out["all"] = {"metric": "TFLOP/s at M=512 (q_k_v, gate_up, down; %s -> fp32)" % ops,
                   "value": round(tf, 1), "unit": "TFLOP/s",
                   "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16, "unit": "TFLOP/s",
                                "frac": round(tf / bf16, 4), "peak_source": peak_src + " (bf16 burst; fp16 dense rate is the same)"}}
     return out
+
+
+def run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank):
+    """The bf16 layer (scales, x, W, y in bf16) on the same workloads: the 24-launch decode step
+    at M=1 (GB/s of packed weights + x + y) and the M=512 prefill shapes (TFLOP/s)."""
+    layers = []
+    with torch.cuda.stream(stream):
+        for li in range(LAYERS):
+            lin = []
+            for name, K, N in DECODE_SHAPES:
+                h = inputs.make_weights(K, N, G, seed=5000 + 1000 * rank + 10 * li + len(lin), dtype="bf16")
+                qw = torch.from_numpy(h["qweight"]).to(dev)
+                qz = torch.from_numpy(h["qzeros"]).to(dev)
+                sc = torch.from_numpy(h["scales"].view(np.int16)).to(dev).view(torch.bfloat16)
+                lin.append((name, K, N, w4.repack(qw, qz, sc, K, N, G, stream=stream)))
+                del qw, qz, sc
+            layers.append(lin)
+    stream.synchronize()
+    M = 1
+    launches = [(name, K, N, packed) for lin in layers for (name, K, N, packed) in lin]
+    xs = [_x_on_device(torch, dev, M, K, i, "bf16") for i, (_, K, _, _) in enumerate(launches)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (_, _, N, _) in launches]
+    step_bytes = sum(alg_bytes(M, K, N) for (_, K, N, _) in launches)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for (_, K, N, packed), x, y in zip(launches, xs, ys):
+            w4.gemm(x, packed, M, N, K, G, y=y, stream=stream)
+    stream.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        for (_, K, N, packed), x, y in zip(launches, xs, ys):
+            w4.gemm(x, packed, M, N, K, G, y=y, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def rep():
+        with torch.cuda.stream(stream):
+            graph.replay()
+    reps = max(20, args.steps)
+    ms = timed(rep, reps) / reps
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src, dtype="bf16")
+    if w4.last_device_error(stream) != 0:
+        raise RuntimeError("device-side error in the bf16 runs")
+    return {"decode": {"metric": "decode-step weight-stream bandwidth, bf16 layer (M=1, %d launches)" % len(launches),
+                       "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                    "frac": round(gbs / hbm, 4), "peak_source": peak_src}},
+            "prefill": prefill}
 
 
 # -------------------------------------------------------------------------------- reference

@@ -4,7 +4,8 @@
  *   y[M,N] = x[M,K] . W,   W[k,n] = (q[k,n] - z[k/g,n]) * s[k/g,n]
  *
  * q and z are 4-bit codes (0..15) packed eight to an int32 along N in the AWQ checkpoint order,
- * s is fp16, x and y are fp16, and one group covers g consecutive rows of K.
+ * s is fp16, x and y are fp16, and one group covers g consecutive rows of K.  The *_bf16 entry
+ * points are the same layer with s, x, W and y in bfloat16.
  *
  * Where the operations come from:
  *  - "Carga de capas cuantizadas: AWQ / GPTQ / Marlin / fp8" (vLLM architecture walkthrough):
@@ -42,6 +43,8 @@
  *    A status other than W4A16_OK means nothing was launched.  Errors raised on the device
  *    (a packed buffer whose header does not match the call's K, N, g, or a bounded wait that
  *    ran out) are recorded in a per-device error word read by w4a16_last_device_error.
+ *    A packed buffer's header also records the element type it was packed for (fp16 or
+ *    bf16), and the calls of the other type reject it the same way.
  */
 #ifndef W4A16_GB300_H
 #define W4A16_GB300_H
@@ -70,7 +73,7 @@ extern "C" {
  * Packed layout, version 1 (own design; the layouts of the pages' other kernels are prior
  * art).  All offsets in bytes from the start of the buffer.
  *   [0, 256)      header: uint32 magic 0x36314134, uint32 version, int32 K, int32 N, int32 g,
- *                 then zeros.
+ *                 int32 dtype (0: fp16 layer, 1: bf16 layer), then zeros.
  *   [256, ...)    NB = ceil(N/64) n-blocks, each of KT = ceil(K/128) chunks of
  *                 CB = 4096 + (128/g) * 160 bytes; chunk (b, t) starts at 256 + (b*KT + t)*CB
  *                 and covers columns [64b, 64b+64) and rows k in [128t, 128t+128).
@@ -78,7 +81,8 @@ extern "C" {
  *                 128 consecutive k as 16 little-endian uint32 words.  Word w holds
  *                 k = 128t + 8w + {0,2,4,6,1,3,5,7}[j] in nibble slot j (bits 4j..4j+3).
  *   chunk meta    [4096, CB): for each of the 128/g groups l of the chunk, 160 bytes:
- *                 64 fp16 scales then 32 bytes of zero codes, both in "lane order": position
+ *                 64 scales (the layer's fp16 or bf16) then 32 bytes of zero codes, both in
+ *                 "lane order": position
  *                 p = 8*(r%8) + 2*(r/16) + (r/8)%2 holds column-row r; the zero of position p
  *                 is nibble p%8 (bits 4(p%8)..) of little-endian uint32 word p/8.
  *   padding       columns n >= N and rows k >= K have code 0, zero code 0 and scale +0.0, so
@@ -190,6 +194,29 @@ int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, int N, int 
  * Changes what w4a16_workspace_bytes reports for split-K problems: size workspaces after
  * setting it.  Not a per-call or per-thread setting: set it before issuing work. */
 int w4a16_set_option(int option, int value);
+
+/* The bfloat16 layer.  Same operation, shapes, layout, alignment and error behaviour as the
+ * entry point without the suffix, with the scales, x, the weights W and y in bfloat16 (bits as
+ * uint16) instead of fp16: W = bf16((q - z) * s) with one round-to-nearest-even rounding, and
+ * y accumulated in fp32 and rounded once to bf16.  The pages' own CPU path computes in bf16
+ * (vllm-omni commit "Add cpu_int4, an asymmetric 4-bit weight path for vLLM's CPU backend":
+ * wider batches unpack the weight to bf16 once, and bf16 is the reference it is measured
+ * against).  A buffer packed by w4a16_repack_bf16 / w4a16_repack_chunk_bf16 records dtype 1 in
+ * its header and is accepted only by the *_bf16 calls (and an fp16 buffer only by the others):
+ * a mismatch is a device-side error and nothing is written.  M <= 32 takes the decode path
+ * (bf16 mma.sync), larger M the tensor-core path (tcgen05 kind::f16 with bf16 operands); the
+ * workspace is that of w4a16_workspace_bytes. */
+int w4a16_repack_bf16(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                      int K, int N, int g, void *packed, void *stream);
+int w4a16_repack_chunk_bf16(const int32_t *qweight_c, int64_t ld_qweight,
+                            const int32_t *qzeros_c, int64_t ld_qzeros,
+                            const uint16_t *scales_c, int64_t ld_scales,
+                            int K, int N, int g, int n0, int n1, void *packed, void *stream);
+int w4a16_gemm_bf16(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+                    void *workspace, size_t workspace_bytes, void *stream);
+int w4a16_dequant_bf16(const void *packed, int K, int N, int g, uint16_t *W, void *stream);
+int w4a16_embed_bf16(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                     void *stream);
 
 /* Static description of a status code. */
 const char *w4a16_status_string(int status);

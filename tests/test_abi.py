@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import __graft_entry__
@@ -143,3 +144,36 @@ def test_awq_to_standard_host_validation(L):
     assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 128, P2, P, NUL) == binding.ERR_MISALIGNED
     assert L.w4a16_awq_to_standard(P, P2, 2048, 3072, 128, P, P, NUL) == binding.ERR_MISALIGNED
     assert L.w4a16_awq_to_standard(P, P, 2048, 3072, 128, ctypes.c_void_p(0x10004), P, NUL) == binding.ERR_MISALIGNED
+
+
+def test_bf16_entry_points_host_validation(L):
+    # the bf16 entry points validate exactly as their fp16 counterparts (rejected before any launch)
+    assert L.w4a16_gemm_bf16(P, P, 1, 2048, 2048, 100, P, NUL, 0, NUL) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_gemm_bf16(P, P, -1, 2048, 2048, 128, P, NUL, 0, NUL) == binding.ERR_INVALID
+    assert L.w4a16_gemm_bf16(NUL, P, 1, 2048, 2048, 128, P, NUL, 0, NUL) == binding.ERR_INVALID
+    assert L.w4a16_gemm_bf16(P_ODD, P, 1, 2048, 2048, 128, P, NUL, 0, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_gemm_bf16(P, P, 0, 2048, 2048, 128, NUL, NUL, 0, NUL) == binding.OK
+    assert L.w4a16_repack_bf16(P, P, P, 2048, 2048, 96, P, NUL) == binding.ERR_UNSUPPORTED
+    assert L.w4a16_repack_bf16(P, P, P, 2048, 2048, 128, P_ODD, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_repack_chunk_bf16(P, 256, P, 256, P, 2048, 2048, 2048, 128, 32, 128, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_repack_chunk_bf16(P, 7, P, 8, P, 64, 2048, 2048, 128, 0, 64, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_dequant_bf16(P, 2048, 2048, 64, NUL, NUL) == binding.ERR_INVALID
+    assert L.w4a16_dequant_bf16(P_ODD, 2048, 2048, 64, P, NUL) == binding.ERR_MISALIGNED
+    assert L.w4a16_embed_bf16(P, -1, P, 2048, 2048, 128, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_embed_bf16(NUL, 0, NUL, 2048, 2048, 128, NUL, NUL) == binding.OK
+
+
+def test_bf16_inputs_are_rounded_draws():
+    """The bf16 input recipe: the same draws as fp16, rounded to bfloat16 (bits as uint16)."""
+    from w4a16_group_wise_gb300 import inputs
+    x16 = inputs.make_x(3, 256, seed=4)
+    xb = inputs.make_x(3, 256, seed=4, dtype="bf16")
+    assert xb.dtype == np.uint16 and xb.shape == (3, 256)
+    wide = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # both round the same normal draws: they agree to bf16's precision
+    assert np.all(np.abs(wide - x16.astype(np.float64)) <= 2.0 ** -8 * np.abs(x16.astype(np.float64)) + 1e-3)
+    h = inputs.make_weights(256, 64, 128, seed=1, dtype="bf16")
+    hf = inputs.make_weights(256, 64, 128, seed=1)
+    assert np.array_equal(h["qweight"], hf["qweight"]) and np.array_equal(h["qzeros"], hf["qzeros"])
+    s = (h["scales"].astype(np.uint32) << 16).view(np.float32)
+    assert np.all((s >= 0.002 * (1 - 2 ** -8)) & (s <= 0.02 * (1 + 2 ** -8)))

@@ -41,7 +41,15 @@ SIGNATURES = {
     "w4a16_set_option": ([_I, _I], _I),
     "w4a16_embed": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
     "w4a16_awq_to_standard": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "w4a16_repack_bf16": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "w4a16_repack_chunk_bf16": ([_P, _I64, _P, _I64, _P, _I64, _I, _I, _I, _I, _I, _P, _P], _I),
+    "w4a16_gemm_bf16": ([_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "w4a16_dequant_bf16": ([_P, _I, _I, _I, _P, _P], _I),
+    "w4a16_embed_bf16": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
 }
+
+# element type of a layer -> suffix of its entry points
+_SUFFIX = {torch.float16: "", torch.bfloat16: "_bf16"}
 
 _lib = None
 
@@ -89,7 +97,7 @@ def _ptr(t):
 def _dev(t, dtype, name):
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dtype != dtype:
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
@@ -112,18 +120,23 @@ def workspace_bytes(M, N, K, g):
     return lib().w4a16_workspace_bytes(M, N, K, g)
 
 
+_HALVES = (torch.float16, torch.bfloat16)
+
+
 def repack(qweight, qzeros, scales, K, N, g, packed=None, stream=None):
-    """AWQ qweight int32 [K, N/8], qzeros int32 [K/g, N/8], scales fp16 [K/g, N] -> packed uint8."""
+    """AWQ qweight int32 [K, N/8], qzeros int32 [K/g, N/8], scales fp16 or bf16 [K/g, N] ->
+    packed uint8 (the scales' type is the layer's element type, recorded in the buffer)."""
     _dev(qweight, torch.int32, "qweight")
     _dev(qzeros, torch.int32, "qzeros")
-    _dev(scales, torch.float16, "scales")
+    _dev(scales, _HALVES, "scales")
     nbytes = packed_bytes(K, N, g)
     if nbytes == 0:
         _check("w4a16_packed_bytes", ERR_UNSUPPORTED)
     if packed is None:
         packed = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
-    _check("w4a16_repack", lib().w4a16_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, g,
-                                              _ptr(packed), _stream(stream)))
+    fn = "w4a16_repack" + _SUFFIX[scales.dtype]
+    _check(fn, getattr(lib(), fn)(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, g, _ptr(packed),
+                                  _stream(stream)))
     return packed
 
 
@@ -132,7 +145,10 @@ def repack_chunk(qweight_c, qzeros_c, scales_c, K, N, g, n0, n1, packed, stream=
     for t, name in ((qweight_c, "qweight"), (qzeros_c, "qzeros"), (scales_c, "scales")):
         if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
             raise ValueError("%s slice must be a 2-D CUDA tensor with unit column stride" % name)
-    _check("w4a16_repack_chunk", lib().w4a16_repack_chunk(
+    if scales_c.dtype not in _HALVES:
+        raise ValueError("scales must be float16 or bfloat16")
+    fn = "w4a16_repack_chunk" + _SUFFIX[scales_c.dtype]
+    _check(fn, getattr(lib(), fn)(
         _ptr(qweight_c), qweight_c.stride(0), _ptr(qzeros_c), qzeros_c.stride(0),
         _ptr(scales_c), scales_c.stride(0), K, N, g, n0, n1, _ptr(packed), _stream(stream)))
     return packed
@@ -154,17 +170,18 @@ def default_workspace(nbytes, device):
 
 
 def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
-    """y fp16 [M, N] = x fp16 [M, K] . W(packed)."""
-    _dev(x, torch.float16, "x")
+    """y [M, N] = x [M, K] . W(packed), in the layer's element type (x fp16 or bf16)."""
+    _dev(x, _HALVES, "x")
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    _dev(y, x.dtype, "y")
     need = workspace_bytes(M, N, K, g)
     if need and workspace is None:
         workspace = default_workspace(need, x.device)
     ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check("w4a16_gemm", lib().w4a16_gemm(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y), ws_ptr, ws_len,
-                                          _stream(stream)))
+    fn = "w4a16_gemm" + _SUFFIX[x.dtype]
+    _check(fn, getattr(lib(), fn)(_ptr(x), _ptr(packed), M, N, K, g, _ptr(y), ws_ptr, ws_len, _stream(stream)))
     return y
 
 
@@ -178,21 +195,27 @@ def gemm_noalloc(x, packed, M, N, K, g, y, stream=None):
     return y
 
 
-def dequant(packed, K, N, g, out=None, stream=None):
-    """fp16 W [K, N] from the packed buffer (bit-exact)."""
+def dequant(packed, K, N, g, out=None, stream=None, dtype=torch.float16):
+    """W [K, N] from the packed buffer (bit-exact), in the layer's element type (out's dtype
+    when out is given, else `dtype`)."""
     if out is None:
-        out = torch.empty((K, N), dtype=torch.float16, device=packed.device)
-    _check("w4a16_dequant", lib().w4a16_dequant(_ptr(packed), K, N, g, _ptr(out), _stream(stream)))
+        out = torch.empty((K, N), dtype=dtype, device=packed.device)
+    _dev(out, _HALVES, "out")
+    fn = "w4a16_dequant" + _SUFFIX[out.dtype]
+    _check(fn, getattr(lib(), fn)(_ptr(packed), K, N, g, _ptr(out), _stream(stream)))
     return out
 
 
-def embed(ids, packed, K, N, g, out=None, stream=None):
-    """Rows of the quantized tied embedding: fp16 [T, K], row t = column ids[t] of W."""
+def embed(ids, packed, K, N, g, out=None, stream=None, dtype=torch.float16):
+    """Rows of the quantized tied embedding: [T, K], row t = column ids[t] of W, in the layer's
+    element type (out's dtype when out is given, else `dtype`)."""
     _dev(ids, torch.int32, "ids")
     T = ids.numel()
     if out is None:
-        out = torch.empty((T, K), dtype=torch.float16, device=ids.device)
-    _check("w4a16_embed", lib().w4a16_embed(_ptr(ids), T, _ptr(packed), K, N, g, _ptr(out), _stream(stream)))
+        out = torch.empty((T, K), dtype=dtype, device=ids.device)
+    _dev(out, _HALVES, "out")
+    fn = "w4a16_embed" + _SUFFIX[out.dtype]
+    _check(fn, getattr(lib(), fn)(_ptr(ids), T, _ptr(packed), K, N, g, _ptr(out), _stream(stream)))
     return out
 
 

@@ -63,6 +63,79 @@ int map_launch(cudaError_t e) {
   return W4A16_ERR_CUDA;
 }
 
+// The entry points' bodies, shared by the fp16 and bf16 variants (dtype: kDtypeF16 / kDtypeBf16).
+int repack_chunk_impl(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c, int64_t ld_qzeros,
+                      const uint16_t *scales_c, int64_t ld_scales, int K, int N, int g, int n0, int n1, int dtype,
+                      void *packed, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!qweight_c || !qzeros_c || !scales_c || !packed) return W4A16_ERR_INVALID;
+  if (n0 < 0 || n1 > N || n0 >= n1 || n0 % kBlockN != 0 || (n1 % kBlockN != 0 && n1 != N))
+    return W4A16_ERR_INVALID;
+  int64_t w = (n1 - n0) / 8;
+  if (ld_qweight < w || ld_qzeros < w || ld_scales < (int64_t)(n1 - n0)) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(qweight_c) & 3u) ||
+      (reinterpret_cast<uintptr_t>(qzeros_c) & 3u) || (reinterpret_cast<uintptr_t>(scales_c) & 1u))
+    return W4A16_ERR_MISALIGNED;
+  const int gl = layout_group(K, g);
+  const int gsrc = (g == -1) ? K : g;  // rows of K per row of the source scales and zeros
+  return map_launch(launch_repack(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales, K, N, gl, gsrc,
+                                  dtype, n0, n1, packed, static_cast<cudaStream_t>(stream)));
+}
+
+int repack_impl(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K, int N, int g,
+                int dtype, void *packed, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!qweight || !qzeros || !scales || !packed) return W4A16_ERR_INVALID;
+  if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(packed))
+    return W4A16_ERR_MISALIGNED;
+  return repack_chunk_impl(qweight, N / 8, qzeros, N / 8, scales, N, K, N, g, 0, N, dtype, packed, stream);
+}
+
+int gemm_impl(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype, uint16_t *y,
+              void *workspace, size_t workspace_bytes, void *stream) {
+  if (M < 0) return W4A16_ERR_INVALID;
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!x || !packed || !y) return W4A16_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+  size_t need = M <= kDecodeMaxM ? 0 : gemm_tc_workspace_bytes(M, N, K);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int gl = layout_group(K, g);
+  if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, gl, dtype, y, err, s));
+  return map_launch(launch_gemm_tc(x, packed, M, N, K, gl, dtype, y, err, workspace, s));
+}
+
+int embed_impl(const int32_t *ids, int T, const void *packed, int K, int N, int g, int dtype, uint16_t *out,
+               void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (T < 0) return W4A16_ERR_INVALID;
+  if (T == 0) return W4A16_OK;
+  if (!ids || !packed || !out) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_embed(ids, T, packed, K, N, layout_group(K, g), dtype, out, err,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int dequant_impl(const void *packed, int K, int N, int g, int dtype, uint16_t *W, void *stream) {
+  int st = check_shape(K, N, g);
+  if (st != W4A16_OK) return st;
+  if (!packed || !W) return W4A16_ERR_INVALID;
+  if (!aligned16(packed) || !aligned16(W)) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_dequant(packed, K, N, layout_group(K, g), dtype, W, err, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 // Only the entry points of include/w4a16.h are exported; everything else is hidden.
@@ -83,63 +156,45 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
 int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c,
                        int64_t ld_qzeros, const uint16_t *scales_c, int64_t ld_scales, int K, int N,
                        int g, int n0, int n1, void *packed, void *stream) {
-  int st = check_shape(K, N, g);
-  if (st != W4A16_OK) return st;
-  if (!qweight_c || !qzeros_c || !scales_c || !packed) return W4A16_ERR_INVALID;
-  if (n0 < 0 || n1 > N || n0 >= n1 || n0 % kBlockN != 0 || (n1 % kBlockN != 0 && n1 != N))
-    return W4A16_ERR_INVALID;
-  int64_t w = (n1 - n0) / 8;
-  if (ld_qweight < w || ld_qzeros < w || ld_scales < (int64_t)(n1 - n0)) return W4A16_ERR_INVALID;
-  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(qweight_c) & 3u) ||
-      (reinterpret_cast<uintptr_t>(qzeros_c) & 3u) || (reinterpret_cast<uintptr_t>(scales_c) & 1u))
-    return W4A16_ERR_MISALIGNED;
-  const int gl = layout_group(K, g);
-  const int gsrc = (g == -1) ? K : g;  // rows of K per row of the source scales and zeros
-  return map_launch(launch_repack(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales,
-                                  K, N, gl, gsrc, n0, n1, packed, static_cast<cudaStream_t>(stream)));
+  return repack_chunk_impl(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales, K, N, g, n0, n1,
+                           kDtypeF16, packed, stream);
+}
+
+int w4a16_repack_chunk_bf16(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c,
+                            int64_t ld_qzeros, const uint16_t *scales_c, int64_t ld_scales, int K, int N,
+                            int g, int n0, int n1, void *packed, void *stream) {
+  return repack_chunk_impl(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales, K, N, g, n0, n1,
+                           kDtypeBf16, packed, stream);
 }
 
 int w4a16_repack(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K,
                  int N, int g, void *packed, void *stream) {
-  int st = check_shape(K, N, g);
-  if (st != W4A16_OK) return st;
-  if (!qweight || !qzeros || !scales || !packed) return W4A16_ERR_INVALID;
-  if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(packed))
-    return W4A16_ERR_MISALIGNED;
-  return w4a16_repack_chunk(qweight, N / 8, qzeros, N / 8, scales, N, K, N, g, 0, N, packed,
-                            stream);
+  return repack_impl(qweight, qzeros, scales, K, N, g, kDtypeF16, packed, stream);
+}
+
+int w4a16_repack_bf16(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K,
+                      int N, int g, void *packed, void *stream) {
+  return repack_impl(qweight, qzeros, scales, K, N, g, kDtypeBf16, packed, stream);
 }
 
 int w4a16_gemm(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                void *workspace, size_t workspace_bytes, void *stream) {
-  if (M < 0) return W4A16_ERR_INVALID;
-  int st = check_shape(K, N, g);
-  if (st != W4A16_OK) return st;
-  if (M == 0) return W4A16_OK;
-  if (!x || !packed || !y) return W4A16_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
-  size_t need = w4a16_workspace_bytes(M, N, K, g);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
-  if (need > 0 && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
-  int *err = device_error_word();
-  if (!err) return W4A16_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int gl = layout_group(K, g);
-  if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, gl, y, err, s));
-  return map_launch(launch_gemm_tc(x, packed, M, N, K, gl, y, err, workspace, s));
+  return gemm_impl(x, packed, M, N, K, g, kDtypeF16, y, workspace, workspace_bytes, stream);
+}
+
+int w4a16_gemm_bf16(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  return gemm_impl(x, packed, M, N, K, g, kDtypeBf16, y, workspace, workspace_bytes, stream);
 }
 
 int w4a16_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
                 void *stream) {
-  int st = check_shape(K, N, g);
-  if (st != W4A16_OK) return st;
-  if (T < 0) return W4A16_ERR_INVALID;
-  if (T == 0) return W4A16_OK;
-  if (!ids || !packed || !out) return W4A16_ERR_INVALID;
-  if (!aligned16(packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return W4A16_ERR_MISALIGNED;
-  int *err = device_error_word();
-  if (!err) return W4A16_ERR_CUDA;
-  return map_launch(launch_embed(ids, T, packed, K, N, layout_group(K, g), out, err, static_cast<cudaStream_t>(stream)));
+  return embed_impl(ids, T, packed, K, N, g, kDtypeF16, out, stream);
+}
+
+int w4a16_embed_bf16(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
+                     void *stream) {
+  return embed_impl(ids, T, packed, K, N, g, kDtypeBf16, out, stream);
 }
 
 int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N, int g,
@@ -156,13 +211,11 @@ int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq,
 }
 
 int w4a16_dequant(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
-  int st = check_shape(K, N, g);
-  if (st != W4A16_OK) return st;
-  if (!packed || !W) return W4A16_ERR_INVALID;
-  if (!aligned16(packed) || !aligned16(W)) return W4A16_ERR_MISALIGNED;
-  int *err = device_error_word();
-  if (!err) return W4A16_ERR_CUDA;
-  return map_launch(launch_dequant(packed, K, N, layout_group(K, g), W, err, static_cast<cudaStream_t>(stream)));
+  return dequant_impl(packed, K, N, g, kDtypeF16, W, stream);
+}
+
+int w4a16_dequant_bf16(const void *packed, int K, int N, int g, uint16_t *W, void *stream) {
+  return dequant_impl(packed, K, N, g, kDtypeBf16, W, stream);
 }
 
 const char *w4a16_status_string(int status) {

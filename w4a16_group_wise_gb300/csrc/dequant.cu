@@ -1,10 +1,10 @@
-// dequant.cu -- packed layout -> fp16 W[K][N], bit-exact.
+// dequant.cu -- packed layout -> W[K][N] in the layer's element type (fp16 or bf16), bit-exact.
 //
 // The analogue of _dequantize_from_int4pack (vllm-omni commit "cpu_int4: dequantize prefill
 // weights from the tinygemm layout, not a copy"): decoding the packed layout is a
 // de-interleave, and the result must be bit-exact against the straightforward dequantizer,
 // including an N that does not tile the 64-column block (N = 80).  Every weight is
-// fp16((q - z) * s) with one rounding (see dq.cuh).
+// fp16((q - z) * s), or bf16((q - z) * s) for a bf16 layer, with one rounding (see dq.cuh).
 //
 // One CTA per chunk (64 columns x 128 rows of K): 256 (column-row, 32-k span) units are
 // converted into a shared [128 k][64 n] tile, then written out as 16-byte row segments.
@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kTileLd = kBlockN + 8;  // padded row of the shared tile (halves), 144 bytes
 
+template <class T>
 __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict__ packed, int K, int N,
                                                       int g, int KT, uint16_t *__restrict__ W, int *err) {
   __shared__ __align__(16) uint16_t tile[kTileK][kTileLd];
@@ -29,7 +30,8 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
 
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);
-    bad = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g);
+    bad = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g ||
+           h->dtype != T::kDtype);
     if (bad) atomicOr(err, 1);
   }
 
@@ -40,17 +42,17 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
     const int p = meta_pos(r);
     uint32_t s = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
     uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
-    ZeroBias zb = zero_bias((zw >> (4 * (p % 8))) & 0xFu);
+    ZeroBias zb = T::zb((zw >> (4 * (p % 8))) & 0xFu);
     uint32_t s2 = s * 0x00010001u;
     uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t v[4];
-      word_to_qz(words[w], zb, v);
+      T::qz(words[w], zb, v);
       const int k0 = 32 * span + 8 * w;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        uint32_t wv = hmul2_u32(v[e], s2);
+        uint32_t wv = T::mul2(v[e], s2);
         tile[k0 + 2 * e][r] = (uint16_t)(wv & 0xFFFFu);
         tile[k0 + 2 * e + 1][r] = (uint16_t)(wv >> 16);
       }
@@ -70,11 +72,15 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
 
 }  // namespace
 
-cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W, int *err,
+cudaError_t launch_dequant(const void *packed, int K, int N, int g, int dtype, uint16_t *W, int *err,
                            cudaStream_t stream) {
   int KT = num_ktiles(K);
   dim3 grid(num_nblocks(N), KT);
-  dequant_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint8_t *>(packed), K, N, g, KT, W, err);
+  const uint8_t *p = static_cast<const uint8_t *>(packed);
+  if (dtype == kDtypeBf16)
+    dequant_kernel<Bf16><<<grid, 128, 0, stream>>>(p, K, N, g, KT, W, err);
+  else
+    dequant_kernel<Fp16><<<grid, 128, 0, stream>>>(p, K, N, g, KT, W, err);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,5 @@
-// embed.cu -- gather of the quantized tied embedding: out[t][k] = W[k][ids[t]], fp16, bit-exact.
+// embed.cu -- gather of the quantized tied embedding: out[t][k] = W[k][ids[t]], bit-exact, in the
+// layer's element type (fp16 or bf16).
 //
 // The LM head's packed weight doubles as the embedding table: the head is tied to the
 // embedding (vllm-omni commit "cpu_int4: repack weights in n-blocks, to bound the load-time
@@ -24,6 +25,7 @@ namespace {
 constexpr int kEmbedThreads = 128;
 constexpr int kChunksPerCta = kEmbedThreads / 16;
 
+template <class T>
 __global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const int32_t *__restrict__ ids,
                                                               const uint8_t *__restrict__ packed, int K, int N,
                                                               int g, int KT, uint16_t *__restrict__ out, int *err) {
@@ -32,7 +34,8 @@ __global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const int32_t *__r
   const int w = threadIdx.x % 16;                                // code word of the column row
   const int k0 = c * kTileK + 8 * w;
   const Header *h = reinterpret_cast<const Header *>(packed);
-  const bool hdr_ok = h->magic == kMagic && h->version == kLayoutVersion && h->K == K && h->N == N && h->g == g;
+  const bool hdr_ok = h->magic == kMagic && h->version == kLayoutVersion && h->K == K && h->N == N && h->g == g &&
+                      h->dtype == T::kDtype;
   if (!hdr_ok) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, 1);
     return;  // a mismatched buffer writes nothing
@@ -50,21 +53,24 @@ __global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const int32_t *__r
     const uint32_t s = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
     const uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
     uint32_t v[4];
-    word_to_qz(word, zero_bias((zw >> (4 * (p % 8))) & 0xFu), v);
+    T::qz(word, T::zb((zw >> (4 * (p % 8))) & 0xFu), v);
     const uint32_t s2 = s * 0x00010001u;
-    o = make_uint4(hmul2_u32(v[0], s2), hmul2_u32(v[1], s2), hmul2_u32(v[2], s2), hmul2_u32(v[3], s2));
+    o = make_uint4(T::mul2(v[0], s2), T::mul2(v[1], s2), T::mul2(v[2], s2), T::mul2(v[3], s2));
   }
   *reinterpret_cast<uint4 *>(out + (size_t)t * K + k0) = o;
 }
 
 }  // namespace
 
-cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
-                         int *err, cudaStream_t stream) {
+cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, int dtype,
+                         uint16_t *out, int *err, cudaStream_t stream) {
   const int KT = num_ktiles(K);
   dim3 grid(T, (KT + kChunksPerCta - 1) / kChunksPerCta);
-  embed_kernel<<<grid, kEmbedThreads, 0, stream>>>(ids, static_cast<const uint8_t *>(packed), K, N, g, KT, out,
-                                                   err);
+  const uint8_t *p = static_cast<const uint8_t *>(packed);
+  if (dtype == kDtypeBf16)
+    embed_kernel<Bf16><<<grid, kEmbedThreads, 0, stream>>>(ids, p, K, N, g, KT, out, err);
+  else
+    embed_kernel<Fp16><<<grid, kEmbedThreads, 0, stream>>>(ids, p, K, N, g, KT, out, err);
   return cudaGetLastError();
 }
 

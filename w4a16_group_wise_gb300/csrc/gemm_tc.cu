@@ -27,6 +27,9 @@
 // producers run ahead on the next tile; with a K split every CTA has one tile and all warps
 // take part in adding the partial tiles.  Every wait is bounded: on a timeout the kernel
 // records an error, drains, frees tensor memory and skips the store.
+// A bf16 layer runs the same kernel with T = Bf16 (dq.cuh): bf16 weights bf16((q - z) * s), x
+// loaded as bf16 by the TMA, the bf16 operand type in the instruction descriptor, y rounded to
+// bf16.
 //
 // Measured on GB300 while tuning this pipeline: keeping the A tile out of shared memory lets
 // the ring hold 6 stages at BM = 256; one warp's stage chain (wait, read, convert, store,
@@ -102,9 +105,12 @@ __device__ __forceinline__ uint64_t sw128_desc(const void *p) {
   return ((addr >> 4) & 0x3FFFull) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = n.
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = n; for a
+// bf16 layer the A and B type fields (bits 7..9 and 10..12) hold 1, bf16.
+template <class T>
 __host__ __device__ inline uint32_t idesc_f16(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  const uint32_t ab = T::kDtype == kDtypeBf16 ? (1u << 7) | (1u << 10) : 0u;
+  return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 // As mma_f16 with the A operand (128 rows x 16 k fp16, K-major) in tensor memory.
@@ -208,6 +214,7 @@ struct SplitPlan {
   int *counters;         // [tiles], zero between calls
 };
 
+template <class T>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const uint8_t *__restrict__ packed, int M, int N,
                                                                int K, int g, int KT, int bm, int stages,
@@ -260,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     mbar_init(&accum_bar, 1);
     // the packed buffer must match the call (read-only: no need to wait for the previous kernel)
     const Header *h = reinterpret_cast<const Header *>(packed);
-    flags = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g) ? 1 : 0;
+    flags = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g ||
+             h->dtype != T::kDtype) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {  // the whole warp allocates tensor memory: tmem_cols fp32 columns x 128 lanes
@@ -314,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       // the ring position advances incrementally and the x descriptor is built once: its
       // start-address field counts 16-byte units, so a stage adds stage_bytes / 16 and a 16-k
       // step 2 (shared addresses stay below 256 KB, so the 14-bit field never carries).
-      const uint32_t idesc = idesc_f16(bm);
+      const uint32_t idesc = idesc_f16<T>(bm);
       const uint64_t bdesc0 = sw128_desc(smem + L.b_off);
       const uint32_t bstep = (uint32_t)L.stage_bytes >> 4;
       bool ok = true;
@@ -443,15 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint4 out[8];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const ZeroBias zb = zero_bias((cur.zw[hh] >> (4 * (p % 8))) & 0xFu);
+        const ZeroBias zb = T::zb((cur.zw[hh] >> (4 * (p % 8))) & 0xFu);
         const uint32_t s2 = cur.sc[hh] * 0x00010001u;
         const uint32_t words[4] = {cur.h[hh].x, cur.h[hh].y, cur.h[hh].z, cur.h[hh].w};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           uint32_t v[4];
-          word_to_qz(words[w], zb, v);
-          out[4 * hh + w] = make_uint4(hmul2_u32(v[0], s2), hmul2_u32(v[1], s2), hmul2_u32(v[2], s2),
-                                       hmul2_u32(v[3], s2));
+          T::qz(words[w], zb, v);
+          out[4 * hh + w] = make_uint4(T::mul2(v[0], s2), T::mul2(v[1], s2), T::mul2(v[2], s2), T::mul2(v[3], s2));
         }
       }
       // every lane has its codes in registers: this group is done with the chunk's slot
@@ -527,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           if (c00 + 16 * b >= bm) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const uint32_t u = h2_as_u32(__floats2half2_rn(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1])));
+            const uint32_t u = T::pack2(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1]));
             const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, u, 1);
             // even lane: row m_{2i} = (own, neighbour) low halves; odd lane: row m_{2i+1} high halves
             const uint32_t w = odd ? __byte_perm(o, u, 0x7632) : __byte_perm(u, o, 0x5410);
@@ -622,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           const int gm = m0 + (eu >> 5), gn = n0 + 4 * (eu & 31);
           if (gm < M && gn < N) {
             uint2 o;
-            o.x = h2_as_u32(__floats2half2_rn(acc.x, acc.y));
-            o.y = h2_as_u32(__floats2half2_rn(acc.z, acc.w));
+            o.x = T::pack2(acc.x, acc.y);
+            o.y = T::pack2(acc.z, acc.w);
             *reinterpret_cast<uint2 *>(y + (size_t)gm * N + gn) = o;
           }
         }
@@ -683,8 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int m = m0 + c0 + j2, n = nq + nn;
         if (m < M && n < N) {
           uint2 o;
-          o.x = h2_as_u32(__floats2half2_rn(acc.x, acc.y));
-          o.y = h2_as_u32(__floats2half2_rn(acc.z, acc.w));
+          o.x = T::pack2(acc.x, acc.y);
+          o.y = T::pack2(acc.z, acc.w);
           *reinterpret_cast<uint2 *>(y + (size_t)m * N + n) = o;
         }
       }
@@ -703,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (c0 >= bm) break;
 #pragma unroll
         for (int j2 = 0; j2 < 16; ++j2)
-          th[j2 * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[b][j2])));
+          th[j2 * 32 + lane] = T::from_float(__uint_as_float(v[b][j2]));
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
@@ -780,7 +787,7 @@ int max_clusters(int splits) {
   std::lock_guard<std::mutex> lock(mu);
   if (!cache[dev][splits]) {
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<Fp16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, 1, splits);
       cfg.blockDim = dim3(kThreads);
@@ -792,7 +799,7 @@ int max_clusters(int splits) {
       attr[0].val.clusterDim.z = splits;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Fp16>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     cache[dev][splits] = n > 0 ? n : -1;
@@ -849,8 +856,11 @@ int set_splitk_mode(int mode) {
   return W4A16_OK;
 }
 
-cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y, int *err,
-                           void *workspace, cudaStream_t stream) {
+namespace {
+
+template <class T>
+cudaError_t launch_gemm_tc_t(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y, int *err,
+                             void *workspace, cudaStream_t stream) {
   const TcPlan P = plan_tc(M, N, K);
   const GemmSmem L = gemm_smem(P.bm, P.stages);
 
@@ -861,7 +871,8 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)P.bm};
   const cuuint32_t es[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
+  const CUtensorMapDataType xtype = T::kDtype == kDtypeBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (enc(&map, xtype, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -881,7 +892,7 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -903,8 +914,16 @@ cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, 
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, static_cast<const uint8_t *>(packed), M, N, K, g,
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T>, map, static_cast<const uint8_t *>(packed), M, N, K, g,
                             num_ktiles(K), P.bm, P.stages, P.tmem_cols, sp, y, err);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype, uint16_t *y,
+                           int *err, void *workspace, cudaStream_t stream) {
+  return dtype == kDtypeBf16 ? launch_gemm_tc_t<Bf16>(x, packed, M, N, K, g, y, err, workspace, stream)
+                             : launch_gemm_tc_t<Fp16>(x, packed, M, N, K, g, y, err, workspace, stream);
 }
 
 }  // namespace w4a16

@@ -32,6 +32,9 @@
 //
 // The warps' partial sums are added in warp order through shared memory, so y is bit-identical
 // from run to run.
+//
+// Every kernel is instantiated for fp16 and for bf16 layers (T = Fp16 / Bf16 of dq.cuh: the
+// nibble conversion, the scale multiply, the mma.sync operand type and the output rounding).
 #include <cuda_runtime.h>
 
 #include "dq.cuh"
@@ -43,15 +46,6 @@ namespace w4a16 {
 namespace {
 
 constexpr int kMaxWarps = 16;
-
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   uint4 v;
@@ -75,7 +69,7 @@ __device__ __forceinline__ uint32_t ld_stream1(const void *p) {
 template <int RT>
 struct Stage {
   uint4 code[RT][2];   // [row-tile][rows r8, r8 + 8], 32 k each
-  uint32_t scale[RT];  // fp16 scales of rows r8 (low half) and r8 + 8 (high half)
+  uint32_t scale[RT];  // scales of rows r8 (low half) and r8 + 8 (high half)
   uint32_t zero[RT];   // zero codes: bits 0..3 row r8, bits 4..7 row r8 + 8
 };
 
@@ -91,7 +85,7 @@ struct XFrag {
 template <int RT, int MB>
 constexpr int kThreadBound = (RT == 1 && MB == 1) ? kMaxWarps * 32 : kMaxWarps * 16;
 
-template <int RT, int MB, bool FACTOR>
+template <class T, int RT, int MB, bool FACTOR>
 __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16_t *__restrict__ x,
                                                               const uint8_t *__restrict__ packed, int M, int N,
                                                               int K, int g, int KT, uint16_t *__restrict__ y,
@@ -113,7 +107,8 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
   int hdr_ok = 1;
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
-    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g);
+    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
+             (h->dtype == T::kDtype);
   }
 
   auto load_w = [&](Stage<RT> &st, int j) {
@@ -169,7 +164,7 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
         Stage<RT> &s = st[d];
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
-          const ZeroBias zb0 = zero_bias(s.zero[r] & 0xFu), zb1 = zero_bias((s.zero[r] >> 4) & 0xFu);
+          const ZeroBias zb0 = T::zb(s.zero[r] & 0xFu), zb1 = T::zb((s.zero[r] >> 4) & 0xFu);
           float dd[MB][4];
 #pragma unroll
           for (int mb = 0; mb < MB; ++mb)
@@ -180,27 +175,27 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
             const uint32_t w0 = (w == 0) ? s.code[r][0].x : (w == 1) ? s.code[r][0].y : (w == 2) ? s.code[r][0].z : s.code[r][0].w;
             const uint32_t w1 = (w == 0) ? s.code[r][1].x : (w == 1) ? s.code[r][1].y : (w == 2) ? s.code[r][1].z : s.code[r][1].w;
             uint32_t v0[4], v1[4];
-            word_to_qz(w0, zb0, v0);
-            word_to_qz(w1, zb1, v1);
+            T::qz(w0, zb0, v0);
+            T::qz(w1, zb1, v1);
             if (!FACTOR) {
               const uint32_t s20 = (s.scale[r] & 0xFFFFu) * 0x00010001u, s21 = (s.scale[r] >> 16) * 0x00010001u;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                v0[e] = hmul2_u32(v0[e], s20);
-                v1[e] = hmul2_u32(v1[e], s21);
+                v0[e] = T::mul2(v0[e], s20);
+                v1[e] = T::mul2(v1[e], s21);
               }
             }
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
               float *dst = FACTOR ? dd[mb] : acc[r][mb];
               const uint4 xw = xc.v[mb][w];
-              mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
-              mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+              T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+              T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
             }
           }
           if (FACTOR) {
-            const float f0 = __half2float(__ushort_as_half((unsigned short)(s.scale[r] & 0xFFFFu)));
-            const float f1 = __half2float(__ushort_as_half((unsigned short)(s.scale[r] >> 16)));
+            const float f0 = T::to_float(s.scale[r] & 0xFFFFu);
+            const float f1 = T::to_float(s.scale[r] >> 16);
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
               acc[r][mb][0] = fmaf(f0, dd[mb][0], acc[r][mb][0]);
@@ -236,7 +231,7 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
     const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = m0 + 8 * mb + 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
-    if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(v));
+    if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
   }
 }
 
@@ -250,7 +245,7 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 constexpr int kSmallRows = 4;   // rows of x per CTA in the lean variant
 constexpr int kSmallWarps = 8;
 
-template <int D, int RT, bool FACTOR>
+template <class T, int D, int RT, bool FACTOR>
 __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
     uint16_t *__restrict__ y, int *err) {
@@ -270,7 +265,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
   int hdr_ok = 1;
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
-    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g);
+    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
+             (h->dtype == T::kDtype);
   }
 
   uint4 code[D][RT][2];
@@ -325,7 +321,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
         const bool xrow = r8 < M;
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
-          const ZeroBias zb0 = zero_bias(zero[d][r] & 0xFu), zb1 = zero_bias((zero[d][r] >> 4) & 0xFu);
+          const ZeroBias zb0 = T::zb(zero[d][r] & 0xFu), zb1 = T::zb((zero[d][r] >> 4) & 0xFu);
           float dd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
@@ -333,24 +329,24 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
             const uint32_t w0 = (w == 0) ? c0.x : (w == 1) ? c0.y : (w == 2) ? c0.z : c0.w;
             const uint32_t w1 = (w == 0) ? c1.x : (w == 1) ? c1.y : (w == 2) ? c1.z : c1.w;
             uint32_t v0[4], v1[4];
-            word_to_qz(w0, zb0, v0);
-            word_to_qz(w1, zb1, v1);
+            T::qz(w0, zb0, v0);
+            T::qz(w1, zb1, v1);
             if (!FACTOR) {
               const uint32_t s20 = (scale[d][r] & 0xFFFFu) * 0x00010001u, s21 = (scale[d][r] >> 16) * 0x00010001u;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                v0[e] = hmul2_u32(v0[e], s20);
-                v1[e] = hmul2_u32(v1[e], s21);
+                v0[e] = T::mul2(v0[e], s20);
+                v1[e] = T::mul2(v1[e], s21);
               }
             }
             const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
             float *dst = FACTOR ? dd : acc[r];
-            mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
-            mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+            T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+            T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
           }
           if (FACTOR) {
-            const float f0 = __half2float(__ushort_as_half((unsigned short)(scale[d][r] & 0xFFFFu)));
-            const float f1 = __half2float(__ushort_as_half((unsigned short)(scale[d][r] >> 16)));
+            const float f0 = T::to_float(scale[d][r] & 0xFFFFu);
+            const float f1 = T::to_float(scale[d][r] >> 16);
             acc[r][0] = fmaf(f0, dd[0], acc[r][0]);
             acc[r][1] = fmaf(f0, dd[1], acc[r][1]);
             acc[r][2] = fmaf(f1, dd[2], acc[r][2]);
@@ -385,7 +381,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
     const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
-    if (m < M && n < N) y[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(v));
+    if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
   }
 }
 
@@ -403,7 +399,7 @@ int sm_count() {
   return count[dev];
 }
 
-template <int RT, int MB, bool FACTOR>
+template <class T, int RT, int MB, bool FACTOR>
 cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, const uint8_t *packed, int M, int N,
                            int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
   const int smem = W * RT * MB * 4 * 32 * 4;
@@ -411,7 +407,7 @@ cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, con
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<RT, MB, FACTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, RT, MB, FACTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          160 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -426,20 +422,20 @@ cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<RT, MB, FACTOR>, x, packed, M, N, K, g, KT, y, err);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<T, RT, MB, FACTOR>, x, packed, M, N, K, g, KT, y, err);
 }
 
-template <int RT>
+template <class T, int RT>
 cudaError_t launch_rt(int tiles, int mblocks, int W, int MB, bool factor, const uint16_t *x, const uint8_t *p,
                       int M, int N, int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
   if (MB == 1)
-    return factor ? launch_variant<RT, 1, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
-                  : launch_variant<RT, 1, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
-  return factor ? launch_variant<RT, 2, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
-                : launch_variant<RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
+    return factor ? launch_variant<T, RT, 1, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
+                  : launch_variant<T, RT, 1, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
+  return factor ? launch_variant<T, RT, 2, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
+                : launch_variant<T, RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
 }
 
-template <int D, int RT>
+template <class T, int D, int RT>
 cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
                          int KT, uint16_t *y, int *err, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -452,14 +448,13 @@ cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, RT, true>, x, p, M, N, K, g, KT, y, err)
-                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<D, RT, false>, x, p, M, N, K, g, KT, y, err);
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, true>, x, p, M, N, K, g, KT, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, false>, x, p, M, N, K, g, KT, y, err);
 }
 
-}  // namespace
-
-cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
-                        int *err, cudaStream_t stream) {
+template <class T>
+cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
+                          int *err, cudaStream_t stream) {
   const int KT = num_ktiles(K);
   const int MB = (M <= 8) ? 1 : 2;
   const int mblocks = (M + 8 * MB - 1) / (8 * MB);
@@ -473,8 +468,8 @@ cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int
   if (M <= kSmallRows && !long_k) {
     // one-tile CTAs (4 per SM) while they fit in one wave; two-tile CTAs (3 per SM) beyond, so
     // that every CTA is resident and has issued all its weight loads when the wait ends
-    if (ctas1 <= 4L * sm_count()) return launch_small<2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
-    return launch_small<2, 2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+    if (ctas1 <= 4L * sm_count()) return launch_small<T, 2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+    return launch_small<T, 2, 2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
   }
   // Two row-tiles per CTA once the grid would cover the GPU several times over (a 2-tile CTA
   // never straddles an n-block: tiles come in fours per n-block and pairs start at even tiles);
@@ -483,8 +478,16 @@ cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int
   const int sms = sm_count();
   const bool two = ctas1 >= (MB == 1 ? 4L : 1L) * sms;
   const int W = (ctas1 >= 4L * sms) ? 4 : (!two && long_k && MB == 1) ? 16 : 8;
-  if (two) return launch_rt<2>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
-  return launch_rt<1>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+  if (two) return launch_rt<T, 2>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+  return launch_rt<T, 1>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype, uint16_t *y,
+                        int *err, cudaStream_t stream) {
+  return dtype == kDtypeBf16 ? launch_gemv_t<Bf16>(x, packed, M, N, K, g, y, err, stream)
+                             : launch_gemv_t<Fp16>(x, packed, M, N, K, g, y, err, stream);
 }
 
 }  // namespace w4a16

@@ -8,34 +8,38 @@
 
 namespace w4a16 {
 
+// `dtype` below is the layer's element type (kDtypeF16 or kDtypeBf16 of layout.cuh): that of x,
+// the scales, the dequantized weights and y, all 16-bit.  Kernels check it against the packed
+// header's dtype word.
+
 // Repack columns [n0, n1) of AWQ tensors (slices starting at column n0, row strides in
 // elements) into their n-blocks of `packed`, and write the header.  g is the layout's group
 // size (32, 64, 128); the source tensors' scales and zeros have one row per gsrc rows of K
 // (gsrc == g, or gsrc == K for one group over all of K).
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
-                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
-                          int n1, void *packed, cudaStream_t stream);
+                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
+                          int n0, int n1, void *packed, cudaStream_t stream);
 
-// packed -> fp16 W[K][N].
-cudaError_t launch_dequant(const void *packed, int K, int N, int g, uint16_t *W, int *err,
+// packed -> W[K][N].
+cudaError_t launch_dequant(const void *packed, int K, int N, int g, int dtype, uint16_t *W, int *err,
                            cudaStream_t stream);
 
 // Decode path: y = x . W for 1 <= M (rows are processed 16 at a time).
-cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g,
+cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype,
                         uint16_t *y, int *err, cudaStream_t stream);
 
 // Tensor-core path (tcgen05): y = x . W for M > kDecodeMaxM.  `workspace` holds
 // gemm_tc_workspace_bytes(M, N, K) bytes (may be null when that is 0); its counters must be zero
 // before the first call and are left zero by every completed call.
-cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
-                           int *err, void *workspace, cudaStream_t stream);
+cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype,
+                           uint16_t *y, int *err, void *workspace, cudaStream_t stream);
 size_t gemm_tc_workspace_bytes(int M, int N, int K);
 // W4A16_SPLITK_AUTO or W4A16_SPLITK_GLOBAL (include/w4a16.h); returns a W4A16 status.
 int set_splitk_mode(int mode);
 
-// Tied-embedding gather: out[t][k] = fp16 W[k][ids[t]] for t < T (grid T x ceil(KT / 8)).
-cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
-                         int *err, cudaStream_t stream);
+// Tied-embedding gather: out[t][k] = W[k][ids[t]] for t < T (grid T x ceil(KT / 8)).
+cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, int dtype,
+                         uint16_t *out, int *err, cudaStream_t stream);
 
 // AWQ -> GPTQ-style standard packing: qweight [K/8][N] packed along K in plain order, qzeros
 // [zero_rows][N/8] in plain order along N.

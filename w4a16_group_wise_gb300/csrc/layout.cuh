@@ -4,7 +4,7 @@
 // self-contained chunks.  Chunk (b, t) covers columns [64b, 64b+64) and rows [128t, 128t+128):
 //   codes  4096 B: 64 column-rows x 64 B; row r (column 64b+r) holds 128 consecutive k as 16
 //          uint32 words; word w holds k = 128t + 8w + kSlotK[j] in nibble slot j.
-//   meta   (128/g) x 160 B: per group, 64 fp16 scales then 64 zero nibbles, in lane order
+//   meta   (128/g) x 160 B: per group, 64 scales (fp16 or bf16) then 64 zero nibbles, in lane order
 //          (position p = 8*(r%8) + 2*(r/16) + (r/8)%2 holds column-row r).
 //
 // Why this shape (GB300 reasoning, not taken from any page):
@@ -44,9 +44,13 @@ __host__ __device__ inline int num_ktiles(int K) { return (K + kTileK - 1) / kTi
 // lane-order position of column-row r (0..63) inside a group's meta
 __host__ __device__ inline int meta_pos(int r) { return 8 * (r % 8) + 2 * (r / 16) + (r / 8) % 2; }
 
+// dtype: element type of x, the scales, the weights and y -- 0 fp16, 1 bf16 (the codes and the
+// zero nibbles do not depend on it).  The rest of the 256 bytes is zero.
 struct Header {
   uint32_t magic, version;
-  int32_t K, N, g;
+  int32_t K, N, g, dtype;
 };
+constexpr int kDtypeF16 = 0;
+constexpr int kDtypeBf16 = 1;
 
 }  // namespace w4a16

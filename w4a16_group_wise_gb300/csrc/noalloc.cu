@@ -26,6 +26,7 @@
 
 #include "../../include/w4a16.h"
 #include "kernels.h"
+#include "layout.cuh"
 
 using namespace w4a16;
 
@@ -75,8 +76,8 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, 
   if (!scratch || !err) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int gl = layout_group(K, g);
-  cudaError_t e = (M <= kDecodeMaxM) ? launch_gemv(x, packed, M, N, K, gl, y, err, s)
-                                     : launch_gemm_tc(x, packed, M, N, K, gl, y, err, scratch, s);
+  cudaError_t e = (M <= kDecodeMaxM) ? launch_gemv(x, packed, M, N, K, gl, kDtypeF16, y, err, s)
+                                     : launch_gemm_tc(x, packed, M, N, K, gl, kDtypeF16, y, err, scratch, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;

@@ -2,7 +2,8 @@
 //
 // Input (vLLM walkthrough "Carga de capas cuantizadas: AWQ / GPTQ / Marlin / fp8", section
 // "Flujo de datos"): qweight int32 [K][N/8] and qzeros int32 [K/g][N/8], both packed along the
-// output dimension; scales fp16 [K/g][N].  AWQ puts column 8c + {0,2,4,6,1,3,5,7}[j] of a word
+// output dimension; scales fp16 [K/g][N] (bf16 for a bf16 layer: the scales are copied as
+// 16-bit patterns, so only the header's dtype word differs).  AWQ puts column 8c + {0,2,4,6,1,3,5,7}[j] of a word
 // in nibble slot j (the "non-standard packing order along the output dimension" of section
 // "Motivacion de diseno").  This is the analogue of process_weights_after_loading: done once,
 // on the device, with no int32 expansion of the codes (vllm-omni commit "cpu_int4: repack
@@ -24,8 +25,8 @@ __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 *
 
 __global__ void __launch_bounds__(256) repack_kernel(
     const int32_t *__restrict__ qweight, int64_t ldq, const int32_t *__restrict__ qzeros,
-    int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
-    int b0, int KT, uint8_t *__restrict__ packed) {
+    int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
+    int n0, int b0, int KT, uint8_t *__restrict__ packed) {
   const int b = b0 + blockIdx.x;  // n-block
   const int t = blockIdx.y;       // k-tile
   const int kb = t * kTileK;
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(256) repack_kernel(
       case 2: v = (uint32_t)K; break;
       case 3: v = (uint32_t)N; break;
       case 4: v = (uint32_t)g; break;
+      case 5: v = (uint32_t)dtype; break;
       default: v = 0;
     }
     reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
@@ -105,14 +107,14 @@ __global__ void __launch_bounds__(256) repack_kernel(
 }  // namespace
 
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
-                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int n0,
-                          int n1, void *packed, cudaStream_t stream) {
+                          const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
+                          int n0, int n1, void *packed, cudaStream_t stream) {
   int b0 = n0 / kBlockN;
   int b1 = (n1 + kBlockN - 1) / kBlockN;
   int KT = num_ktiles(K);
   dim3 grid(b1 - b0, KT);
-  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, n0, b0,
-                                          KT, static_cast<uint8_t *>(packed));
+  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0,
+                                          b0, KT, static_cast<uint8_t *>(packed));
   return cudaGetLastError();
 }
 

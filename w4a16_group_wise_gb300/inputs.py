@@ -12,6 +12,8 @@ Recipe (numpy PCG64; one independent sub-stream per tensor from a SeedSequence k
   - scales fp16 [K/g, N]: uniform on [lo, hi] (default [0.002, 0.02]) or log-uniform on
     [lo, hi] (``scale_dist="loguniform"``, e.g. [1e-4, 0.1]), rounded to fp16 by numpy.
   - x fp16 [M, K]: standard normal, rounded to fp16 by numpy.
+  - bf16 layers (``dtype="bf16"``): the same draws, scales and x rounded to bfloat16 by torch
+    (nearest even) and returned as uint16 bit patterns, numpy having no bfloat16 type.
 Shapes follow the pages' layers: K = 2048 hidden, q_k_v N = 3072, gate_up N = 13312,
 down K = 6656 / N = 2048, tied embedding / LM head N = 131072, and the N = 80 tail case.
 """
@@ -25,9 +27,17 @@ def _rng(seed, tag, *shape):
     return np.random.Generator(np.random.PCG64(ss))
 
 
+def bf16_bits(a):
+    """float array -> bfloat16 bit patterns (uint16 array of the same shape), rounded by torch."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 def make_weights(K, N, g, seed=0, zeros="uniform", scale_dist="uniform", scale_lo=0.002,
-                 scale_hi=0.02):
-    """AWQ-format tensors of one layer: dict(qweight int32, qzeros int32, scales float16)."""
+                 scale_hi=0.02, dtype="f16"):
+    """AWQ-format tensors of one layer: dict(qweight int32, qzeros int32, scales) with scales
+    float16, or (dtype="bf16") bfloat16 bits as uint16."""
     if N % 8 or K % g:
         raise ValueError("N must be a multiple of 8 and K a multiple of g")
     G = K // g
@@ -47,12 +57,14 @@ def make_weights(K, N, g, seed=0, zeros="uniform", scale_dist="uniform", scale_l
         s = np.exp(r.uniform(np.log(scale_lo), np.log(scale_hi), size=(G, N)))
     else:
         raise ValueError(scale_dist)
-    return {"qweight": qweight, "qzeros": qzeros, "scales": s.astype(np.float16)}
+    scales = bf16_bits(s) if dtype == "bf16" else s.astype(np.float16)
+    return {"qweight": qweight, "qzeros": qzeros, "scales": scales}
 
 
-def make_x(M, K, seed=0):
-    """Activations fp16 [M, K], standard normal."""
-    return _rng(seed, "x", M, K).standard_normal((M, K)).astype(np.float16)
+def make_x(M, K, seed=0, dtype="f16"):
+    """Activations [M, K], standard normal: fp16, or (dtype="bf16") bfloat16 bits as uint16."""
+    x = _rng(seed, "x", M, K).standard_normal((M, K))
+    return bf16_bits(x) if dtype == "bf16" else x.astype(np.float16)
 
 
 # Layer shapes (K, N) of the pages' model.
