@@ -4,22 +4,23 @@
 // activations is linear in the batch (12.9x slower than bf16 at 512 rows), so wide batches
 // unpack the weight once and run an ordinary dense GEMM (vllm-omni commit "Add cpu_int4, an
 // asymmetric 4-bit weight path for vLLM's CPU backend").  Here the unpacking is fused into the
-// GEMM: each 128 x 64 weight tile is dequantized once per CTA into tensor memory and consumed
+// GEMM: each 128 x 128 weight tile is dequantized once per CTA into tensor memory and consumed
 // by the 5th-generation tensor cores (tcgen05.mma, fp16 x fp16 -> fp32 in tensor memory); no
 // dequantized W ever reaches HBM.
 //
 // Orientation: D[n][m] = sum_k W^T[n][k] * x^T[k][m], i.e. the MMA's M dimension (128) runs
 // over output columns n and its N dimension (BM <= 256) over rows m of x, so few rows of x
-// waste no tensor work.  Roles, per 64-k stage of a ring of up to 8 stages:
+// waste no tensor work.  Roles, per 128-k stage (one packed chunk) of a ring of up to 4 stages:
 //  - one lane of warp 2 copies the packed chunks of the tile's two n-blocks (codes and their
 //    scales and zeros, contiguous in the packed layout) into a ring of shared-memory slots with
 //    bulk asynchronous copies, one 128-k chunk per slot;
-//  - one lane of warp 0 loads the x tile (BM rows x 64 k, fp16) with a TMA copy into a
-//    128-byte-swizzled K-major tile (rows past M and k past K read as 0);
-//  - warps 4..11, in two groups taking alternate stages (one lane per column-row), read the
-//    codes from the slot, convert them to the exact fp16 weights fp16((q - z) * s) (dq.cuh) and
-//    store them into the stage's A tile in tensor memory (tcgen05.st);
-//  - one lane of warp 1 issues 4 MMAs (K = 16 each, A from tensor memory, x from shared
+//  - one lane of warp 0 loads the x tile (BM rows x 128 k, fp16) with two TMA copies into two
+//    128-byte-swizzled K-major atoms of 64 k (rows past M and k past K read as 0);
+//  - warps 4..11, in two groups taking the two 64-k halves of every stage (one lane per
+//    column-row), read the codes from the slot, convert them to the exact fp16 weights
+//    fp16((q - z) * s) (dq.cuh) and store them into the stage's A tile in tensor memory
+//    (tcgen05.st);
+//  - one lane of warp 1 issues 8 MMAs (K = 16 each, A from tensor memory, x from shared
 //    memory) once both operands are in place and commits them to the stage's "empty" barrier,
 //    which frees the stage when they complete.
 // Without a K split the CTAs are persistent (one per SM, walking the tiles) and warps 12..15
@@ -32,11 +33,13 @@
 // bf16.
 //
 // Measured on GB300 while tuning this pipeline: keeping the A tile out of shared memory lets
-// the ring hold 6 stages at BM = 256; one warp's stage chain (wait, read, convert, store,
+// the ring hold 384 k at BM = 256; one warp's chain for 64 k (wait, read, convert, store,
 // arrive) takes ~1200 cycles against ~670 cycles of MMAs, hence two converting groups; the
-// MMA-issuing lane is on the critical path of every stage, so its loop does no divisions and
-// builds no descriptors; and prefetching code chunks into L2 with bulk prefetches slowed the
-// kernel once the rest was tuned (the copies compete for the same copy engine).
+// MMA-issuing lane is on the critical path of every stage (~600 cycles of barrier wait, issue
+// and commit per 4 MMAs), so its loop does no divisions and builds no descriptors, and a stage
+// spans a whole chunk, so that one barrier round trip feeds 8 MMAs; and prefetching code chunks
+// into L2 with bulk prefetches slowed the kernel once the rest was tuned (the copies compete
+// for the same copy engine).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -56,10 +59,11 @@ namespace w4a16 {
 namespace {
 
 constexpr int kBN = 128;                      // weight rows (output columns n) per CTA = MMA M
-constexpr int kBK = 64;                       // k per stage: one 128-byte swizzle atom of fp16
-constexpr int kMaxStages = 8;
+constexpr int kBK = 64;                       // k per 128-byte swizzle atom of fp16
+constexpr int kStageK = 128;                  // k per stage: one packed chunk, two atoms
+constexpr int kMaxStages = 4;
 // Tensor memory (512 columns x 128 lanes of 32 bits): the fp32 accumulator in columns
-// [0, BM), and the stages' fp16 A tiles (128 column-rows x 64 k = 32 columns each) from
+// [0, BM), and the stages' fp16 A tiles (128 column-rows x 128 k = 64 columns each) from
 // column kATmemCol on.
 constexpr int kTmemCols = 512;
 constexpr int kATmemCol = 256;
@@ -77,17 +81,19 @@ constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 1
 
 struct GemmSmem {
   int stages, bm, cslots;
-  int b_off, stage_bytes, codes_off, total;
+  int b_off, atom_bytes, stage_bytes, codes_off, total;
 };
 
 // [stages x x-tile] [cslots x code slot]; at least 32 KB (the epilogue's transpose buffers
-// reuse the front of it once the rings are idle).  Small x tiles leave room for a deeper code
-// ring: measured, the converting warps otherwise wait for the copies at small BM.
+// reuse the front of it once the rings are idle).  A stage's x tile is two swizzle atoms of
+// BM rows x 64 k, the second at atom_bytes.  Small x tiles leave room for a deeper code ring:
+// measured, the converting warps otherwise wait for the copies at small BM.
 __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   GemmSmem s;
   s.bm = bm;
   s.stages = stages;
-  s.stage_bytes = bm * kBK * 2;
+  s.atom_bytes = bm * kBK * 2;
+  s.stage_bytes = 2 * s.atom_bytes;
   s.b_off = 0;
   s.codes_off = stages * s.stage_bytes;
   int free_slots = (kSmemBudget - s.codes_off) / kCodeSlotBytes;
@@ -197,7 +203,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 // --------------------------------------------------------------------------- the kernel
 
-// Split-K plan: each (n-tile, m-tile) is cut into `splits` consecutive ranges of 64-k stages.
+// Split-K plan: each (n-tile, m-tile) is cut into `splits` consecutive ranges of 128-k stages.
 // With splits > 1 the partial tiles are added in split order, so y does not depend on timing:
 //  - cluster: the splits of a tile form one thread-block cluster; every CTA leaves its fp32
 //    partial tile in its own shared memory and each adds a 1/splits slice of the tile from all
@@ -207,9 +213,9 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 struct SplitPlan {
   int splits;
   int cluster;           // 1: cluster reduction, 0: workspace reduction
-  int persist;           // 1: one CTA per SM walks the tiles, two accumulators (splits == 1)
+  int persist;           // 1: one CTA per SM walks the tiles (splits == 1)
   int ntn, ntm;          // n-tiles and m-tiles of the problem
-  int stages_per_split;  // 64-k stages per split, even (the last split may have fewer)
+  int stages_per_split;  // 128-k stages per split (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
   int *counters;         // [tiles], zero between calls
 };
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
   __shared__ uint64_t cfull_bar[kMaxCodeSlots], cempty_bar[kMaxCodeSlots];
-  __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // the two accumulators of a persistent CTA
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // accumulator hand-off of a persistent CTA ([0])
   __shared__ uint32_t tmem_base;
   __shared__ int flags, last;
 
@@ -233,11 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const GemmSmem L = gemm_smem(bm, stages);
   const int NB = num_nblocks(N);
   const int CB = chunk_bytes(g);
-  const int KS = (K + kBK - 1) / kBK;  // 64-k stages over K (a padded half chunk is skipped)
-  const int st_begin = blockIdx.z * sp.stages_per_split;  // even: a split starts on a chunk
+  const int KS = KT;  // 128-k stages over K: one per chunk (k past K reads as 0 and has code 0)
+  const int st_begin = blockIdx.z * sp.stages_per_split;
   const int nst = max(0, min(KS, st_begin + sp.stages_per_split) - st_begin);
-  const int nch = (nst + 1) / 2;  // 128-k chunks per tile
-  const uint32_t x_bytes = (uint32_t)bm * kBK * 2;
+  const uint32_t x_bytes = (uint32_t)L.stage_bytes;
   uint8_t *codes = smem + L.codes_off;
   // Tiles of this CTA: a persistent CTA takes tiles blockIdx.x, + gridDim.x, ... of the
   // (n-tile, m-tile) grid (m fastest, so neighbouring CTAs share weights); otherwise the one
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full_bar[s], 1 + kDeqWarps / 2);  // TMA expect-tx arrival + one per warp of a group
+      mbar_init(&full_bar[s], 1 + kDeqWarps);  // TMA expect-tx arrival + one per dequant warp
       mbar_init(&empty_bar[s], 1);             // one tcgen05.commit per use
     }
     for (int c = 0; c < L.cslots; ++c) {
@@ -299,7 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         for (int j = 0; j < nst; ++j) {
           if (use > 0 && !(ok = mbar_wait_sleep_bounded(&empty_bar[s], (use - 1) & 1))) break;
           mbar_arrive_expect_tx(&full_bar[s], x_bytes);
-          tma_load_2d(smem + s * L.stage_bytes + L.b_off, &xmap, (st_begin + j) * kBK, m0, &full_bar[s]);
+          uint8_t *xs = smem + s * L.stage_bytes + L.b_off;
+          tma_load_2d(xs, &xmap, (st_begin + j) * kStageK, m0, &full_bar[s]);
+          tma_load_2d(xs + L.atom_bytes, &xmap, (st_begin + j) * kStageK + kBK, m0, &full_bar[s]);
           ++issued;
           if (++s == stages) {
             s = 0;
@@ -321,10 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       // ~670 cycles, and a loop with per-stage divisions and descriptor builds took ~1100), so
       // the ring position advances incrementally and the x descriptor is built once: its
       // start-address field counts 16-byte units, so a stage adds stage_bytes / 16 and a 16-k
-      // step 2 (shared addresses stay below 256 KB, so the 14-bit field never carries).
+      // step 2 and the second atom atom_bytes / 16 (shared addresses stay below 256 KB, so the
+      // 14-bit field never carries).
       const uint32_t idesc = idesc_f16<T>(bm);
       const uint64_t bdesc0 = sw128_desc(smem + L.b_off);
       const uint32_t bstep = (uint32_t)L.stage_bytes >> 4;
+      const uint64_t batom = (uint64_t)((uint32_t)L.atom_bytes >> 4);
       bool ok = true;
       int s = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
@@ -335,12 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         for (int j = 0; j < nst; ++j) {
           if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
           tc_fence_after();
-          const uint32_t a = tmem + (uint32_t)(kATmemCol + 32 * s);
+          const uint32_t a = tmem + (uint32_t)(kATmemCol + 64 * s);
           const uint64_t bd = bdesc0 + (uint64_t)(bstep * (uint32_t)s);
           mma_f16_tmem_a(acc, a, bd, idesc, j > 0 ? 1u : 0u);  // 16 k = 8 columns of A, 32 bytes of x
           mma_f16_tmem_a(acc, a + 8, bd + 2, idesc, 1u);
           mma_f16_tmem_a(acc, a + 16, bd + 4, idesc, 1u);
           mma_f16_tmem_a(acc, a + 24, bd + 6, idesc, 1u);
+          mma_f16_tmem_a(acc, a + 32, bd + batom, idesc, 1u);  // second 64 k: the other atom
+          mma_f16_tmem_a(acc, a + 40, bd + batom + 2, idesc, 1u);
+          mma_f16_tmem_a(acc, a + 48, bd + batom + 4, idesc, 1u);
+          mma_f16_tmem_a(acc, a + 56, bd + batom + 6, idesc, 1u);
           mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
           if (++s == stages) {
             s = 0;
@@ -365,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (lane == 0) {
       auto chunk_src = [&](int it, int lc, int q) {
         const int nb0 = tile_n0(it) >> 6;
-        return packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + (st_begin >> 1) + lc) * CB;
+        return packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + st_begin + lc) * CB;
       };
       auto nblocks = [&](int it) { return ((tile_n0(it) >> 6) + 1 < NB) ? 2 : 1; };
       bool ok = true;
@@ -373,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       int cs = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
         const int nblk = nblocks(it);
-        for (int lc = 0; lc < nch; ++lc) {
+        for (int lc = 0; lc < nst; ++lc) {
           if (use > 0 && !(ok = mbar_wait_sleep_bounded(&cempty_bar[cs], (use - 1) & 1))) break;
           mbar_arrive_expect_tx(&cfull_bar[cs], (uint32_t)(nblk * CB));
           for (int q = 0; q < nblk; ++q)
@@ -392,12 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ------------------------------------------------------------ dequant producers
-    // Two groups of four warps take alternate 64-k stages of every tile (group gsel: stages
-    // gsel, gsel + 2, ...), so two stages are converted at once.  In a group, lane l of warp w
-    // converts column-row r = 32 (w % 4) + l: the 64 k of the stage are 32 code bytes of the
-    // row in the chunk slot (read one stage ahead, before the waits, to hide the shared-memory
-    // latency), giving eight 16-byte pieces of the swizzled A row.  A persistent CTA's tiles
-    // have an even number of stages, so every chunk is read by both groups.
+    // Two groups of four warps take the two 64-k halves of every stage (group gsel: k 64 gsel ..
+    // 64 gsel + 63 of each chunk), so both halves are converted at once and every chunk slot is
+    // read by both groups.  In a group, lane l of warp w converts column-row r = 32 (w % 4) + l:
+    // its 64 k are 32 code bytes of the row in the chunk slot (read one stage ahead, before the
+    // waits, to hide the shared-memory latency), giving 32 columns of the stage's A tile.
     const int gsel = (warp - 4) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int gshift = g == 32 ? 5 : g == 64 ? 6 : 7;  // group of a 32-k span: (32 k32) >> gshift
@@ -408,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint4 h[2];                                 // k 0..31 and 32..63 of the stage
       uint32_t sc[2], zw[2];                      // scale and zero word of each 32-k half
     };
-    // read stage j of a tile from code slot cs (have: the row's n-block exists)
-    auto read_codes = [&](int cs, bool have, int j, Codes &cd) {
+    // read this group's half of a stage from code slot cs (have: the row's n-block exists)
+    auto read_codes = [&](int cs, bool have, Codes &cd) {
       const uint8_t *ch = codes + cs * kCodeSlotBytes + (r >> 6) * CB;  // this row's chunk copy
-      const int k64 = (st_begin + j) & 1;                              // stage half of the chunk
+      const int k64 = gsel;                                            // half of the chunk
       uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;                      // read 0: half rot, read 1: the other
       uint32_t s0 = 0, s1 = 0, z0 = 0, z1 = 0;
       if (have) {
@@ -435,16 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     auto row_has_block = [&](int it) { return (tile_n0(it) >> 6) + (r >> 6) < NB; };
     bool ok = true;
     Codes cur;
-    int it = 0, j = gsel;
+    int it = 0, j = 0;
     // ring positions, advanced incrementally: code slot of the current chunk and its use, stage
-    // slot of the current stage and its use (a group takes every other stage, one per chunk)
-    int cs = (j >> 1) % L.cslots, cuse = 0;
-    int s = j % stages, use = j / stages;
+    // slot of the current stage and its use (one stage per chunk)
+    int cs = 0, cuse = 0;
+    int s = 0, use = 0;
     bool have = row_has_block(0);
-    if (j >= nst) it = my_tiles;  // this group has no stage (one-stage split)
+    if (nst <= 0) it = my_tiles;
     if (it < my_tiles) {
       ok = mbar_wait_bounded(&cfull_bar[cs], cuse & 1);
-      if (ok) read_codes(cs, have, j, cur);
+      if (ok) read_codes(cs, have, cur);
     }
     while (it < my_tiles && ok) {
       // convert this stage's codes into registers
@@ -466,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       if (lane == 0) mbar_arrive(&cempty_bar[cs]);
       // the group's next stage (the next chunk, or the first of the next tile): read it while
       // waiting for the stage buffer
-      int itn = it, jn = j + 2;
+      int itn = it, jn = j + 1;
       if (jn >= nst) {
         ++itn;
-        jn = gsel;
+        jn = 0;
         if (itn < my_tiles) have = row_has_block(itn);
       }
       if (++cs == L.cslots) {
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       if (itn < my_tiles) {
         if (!(ok = mbar_wait_bounded(&cfull_bar[cs], cuse & 1))) break;
-        read_codes(cs, have, jn, cur);
+        read_codes(cs, have, cur);
       }
       if (use > 0 && !(ok = mbar_wait_bounded(&empty_bar[s], (use - 1) & 1))) break;
       tc_fence_after();  // after the MMAs that read this stage's A tile
@@ -493,15 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           v[4 * cc + 2] = out[cc].z;
           v[4 * cc + 3] = out[cc].w;
         }
-        tmem_st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kATmemCol + 32 * s), v);
+        tmem_st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kATmemCol + 64 * s + 32 * gsel), v);
       }
       tc_fence_before();  // the tensor cores read this tile after the barrier
       __syncwarp();
       if (lane == 0) mbar_arrive(&full_bar[s]);
       it = itn;
       j = jn;
-      if ((s += 2) >= stages) {
-        s -= stages;
+      if (++s == stages) {
+        s = 0;
         ++use;
       }
     }
@@ -814,9 +826,9 @@ TcPlan plan_tc(int M, int N, int K) {
   while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= kSmemBudget) ++p.stages;
   p.tmem_cols = kTmemCols;
   p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
-  const int KS = (K + kBK - 1) / kBK;
+  const int KS = num_ktiles(K);  // 128-k stages
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
-  // four 64-k stages per split and at most one cluster's worth of splits.  Where the device runs
+  // two 128-k stages per split and at most one cluster's worth of splits.  Where the device runs
   // clusters, all clusters of the launch must be resident at once (measured: a second wave of
   // clusters costs more than the splits gain), so the split count is lowered until they are;
   // both reductions use the same count, so they add the same partial tiles.
@@ -826,20 +838,19 @@ TcPlan plan_tc(int M, int N, int K) {
   p.splits = 1;
   if (4 * p.tiles < 3 * sms && p.tiles <= kMaxSplitTiles) {
     p.splits = sms / p.tiles;
-    if (p.splits > KS / 4) p.splits = KS / 4;
+    if (p.splits > KS / 2) p.splits = KS / 2;
     if (p.splits > kMaxSplits) p.splits = kMaxSplits;
     if (p.splits < 1) p.splits = 1;
     if (clusters)
       while (p.splits > 1 && max_clusters(p.splits) < p.tiles) --p.splits;
   }
   p.stages_per_split = (KS + p.splits - 1) / p.splits;
-  p.stages_per_split += p.stages_per_split & 1;  // splits start on a 128-k chunk
   p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
   p.cluster = p.splits > 1 && mode != W4A16_SPLITK_GLOBAL && clusters && max_clusters(p.splits) >= p.tiles;
   p.partial_bytes = (p.splits > 1 && !p.cluster) ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
-  // Without a split, one CTA per SM walks the tiles with two accumulators, so that a tile's
-  // epilogue overlaps the next tile's MMAs (tiles then need an even number of stages)
-  p.persist = p.splits == 1 && KS % 2 == 0;
+  // Without a split, one CTA per SM walks the tiles and dedicated epilogue warps drain each
+  // finished accumulator while the producers run ahead on the next tile
+  p.persist = p.splits == 1;
   return p;
 }
 
