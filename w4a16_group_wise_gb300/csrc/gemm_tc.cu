@@ -63,10 +63,10 @@ constexpr int kBK = 64;                       // k per 128-byte swizzle atom of 
 constexpr int kStageK = 128;                  // k per stage: one packed chunk, two atoms
 constexpr int kMaxStages = 4;
 // Tensor memory (512 columns x 128 lanes of 32 bits): the fp32 accumulator in columns
-// [0, BM), and the stages' fp16 A tiles (128 column-rows x 128 k = 64 columns each) from
-// column kATmemCol on.
+// [0, BM) -- or two, [0, BM) and [BM, 2 BM), so that a persistent CTA's epilogue drains one
+// while the MMAs fill the other -- and the stages' fp16 A tiles (128 column-rows x 128 k = 64
+// columns each) in the last 64 x stages columns.
 constexpr int kTmemCols = 512;
-constexpr int kATmemCol = 256;
 // warp 0 x TMA, warp 1 MMA, warp 2 code copies, warps 4..11 dequant, warps 12..15 epilogue of a
 // persistent CTA
 constexpr int kThreads = 512;
@@ -81,11 +81,11 @@ constexpr int kCodeSlotBytes = 9472;  // two n-blocks' chunks, 2 * (4096 + 4 * 1
 
 struct GemmSmem {
   int stages, bm, cslots;
-  int b_off, atom_bytes, stage_bytes, codes_off, total;
+  int b_off, atom_bytes, stage_bytes, codes_off, epi_off, total;
 };
 
-// [stages x x-tile] [cslots x code slot]; at least 32 KB (the epilogue's transpose buffers
-// reuse the front of it once the rings are idle).  A stage's x tile is two swizzle atoms of
+// [stages x x-tile] [cslots x code slot], at least 32 KB (a one-tile CTA's epilogue reuses the
+// front of it once the rings are idle), then 1 KB per persistent epilogue warp.  A stage's x tile is two swizzle atoms of
 // BM rows x 64 k, the second at atom_bytes.  Small x tiles leave room for a deeper code ring:
 // measured, the converting warps otherwise wait for the copies at small BM.
 __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
@@ -100,6 +100,8 @@ __host__ __device__ inline GemmSmem gemm_smem(int bm, int stages) {
   s.cslots = free_slots < kMinCodeSlots ? kMinCodeSlots : free_slots > kMaxCodeSlots ? kMaxCodeSlots : free_slots;
   s.total = s.codes_off + s.cslots * kCodeSlotBytes;
   if (s.total < 32 * 1024) s.total = 32 * 1024;
+  s.epi_off = s.total;  // the persistent epilogue's transpose buffers, 1 KB per warp
+  s.total += kEpiWarps * 1024;
   return s;
 }
 
@@ -214,6 +216,8 @@ struct SplitPlan {
   int splits;
   int cluster;           // 1: cluster reduction, 0: workspace reduction
   int persist;           // 1: one CTA per SM walks the tiles (splits == 1)
+  int dbl;               // 1: two accumulators, alternating by tile (persistent CTAs)
+  int a_col0;            // first tensor-memory column of the stages' A tiles
   int ntn, ntm;          // n-tiles and m-tiles of the problem
   int stages_per_split;  // 128-k stages per split (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], accum_bar;
   __shared__ uint64_t cfull_bar[kMaxCodeSlots], cempty_bar[kMaxCodeSlots];
-  __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // accumulator hand-off of a persistent CTA ([0])
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2];  // accumulator hand-offs of a persistent CTA
   __shared__ uint32_t tmem_base;
   __shared__ int flags, last;
 
@@ -337,14 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       bool ok = true;
       int s = 0, use = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
-        // the accumulator is free once the epilogue warps have read the previous tile's
-        if (sp.persist && it > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[0], (it - 1) & 1))) break;
+        // accumulator ab is free once the epilogue warps have read the last tile that used it
+        const int ab = sp.dbl ? (it & 1) : 0, ause = sp.dbl ? (it >> 1) : it;
+        if (sp.persist && ause > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[ab], (ause - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t acc = tmem;
+        const uint32_t acc = tmem + (uint32_t)(ab * bm);
         for (int j = 0; j < nst; ++j) {
           if (!(ok = mbar_wait_sleep_bounded(&full_bar[s], use & 1))) break;
           tc_fence_after();
-          const uint32_t a = tmem + (uint32_t)(kATmemCol + 64 * s);
+          const uint32_t a = tmem + (uint32_t)(sp.a_col0 + 64 * s);
           const uint64_t bd = bdesc0 + (uint64_t)(bstep * (uint32_t)s);
           mma_f16_tmem_a(acc, a, bd, idesc, j > 0 ? 1u : 0u);  // 16 k = 8 columns of A, 32 bytes of x
           mma_f16_tmem_a(acc, a + 8, bd + 2, idesc, 1u);
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         if (!ok) break;
         // the accumulator is final once every MMA above completes
-        mma_commit(sp.persist ? &tfull_bar[0] : &accum_bar);
+        mma_commit(sp.persist ? &tfull_bar[ab] : &accum_bar);
       }
       if (!ok) {  // let every issued MMA finish before the CTA may exit
         atomicOr(&flags, 2);
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           v[4 * cc + 2] = out[cc].z;
           v[4 * cc + 3] = out[cc].w;
         }
-        tmem_st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kATmemCol + 64 * s + 32 * gsel), v);
+        tmem_st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(sp.a_col0 + 64 * s + 32 * gsel), v);
       }
       tc_fence_before();  // the tensor cores read this tile after the barrier
       __syncwarp();
@@ -521,18 +526,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   } else if (warp >= 4 + kDeqWarps && sp.persist) {
     // ------------------------------------------------------------ persistent epilogue
     // Warp q of the four reads TMEM lanes 32q .. 32q + 31 (column-rows n) of an accumulator
-    // while the MMAs fill the other one; lane pairs swap halves so that each lane stores two
-    // consecutive n of one row m.
+    // (while the MMAs fill the other one, with two), 16 columns (rows m) at a time, rounds them
+    // and turns each 32 n x 16 m block around in its 1 KB of shared memory, so that a lane
+    // stores 16 bytes of consecutive n of one row m (measured: the 4-byte stores of lane pairs
+    // this replaces took ~9,000 cycles per 256-row tile while the MMAs waited).
     const int q = warp & 3;
+    uint16_t *th = reinterpret_cast<uint16_t *>(smem + L.epi_off + q * 1024);
     griddep_wait();  // y may still be read by the previous kernel
     bool ok = true;
     for (int it = 0; it < my_tiles && ok; ++it) {
-      const int ab = 0;
-      if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[0], it & 1))) break;
+      const int ab = sp.dbl ? (it & 1) : 0, ause = sp.dbl ? (it >> 1) : it;
+      if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[ab], ause & 1))) break;
       tc_fence_after();
-      const int n0 = tile_n0(it), m0 = tile_m0(it);
-      const int n = n0 + 32 * q + (lane & ~1);
-      const bool odd = lane & 1;
+      const int n0 = tile_n0(it) + 32 * q, m0 = tile_m0(it);
       const bool store = flags == 0;
       for (int c00 = 0; c00 < bm; c00 += 64) {  // four 16-column groups per wait
         uint32_t v[4][16];
@@ -545,19 +551,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         for (int b = 0; b < 4; ++b) {
           if (c00 + 16 * b >= bm) break;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t u = T::pack2(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1]));
-            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, u, 1);
-            // even lane: row m_{2i} = (own, neighbour) low halves; odd lane: row m_{2i+1} high halves
-            const uint32_t w = odd ? __byte_perm(o, u, 0x7632) : __byte_perm(u, o, 0x5410);
-            const int m = m0 + c00 + 16 * b + 2 * i + (odd ? 1 : 0);
-            if (store && m < M && n < N) *reinterpret_cast<uint32_t *>(y + (size_t)m * N + n) = w;
+          for (int j2 = 0; j2 < 16; ++j2) th[j2 * 32 + lane] = T::from_float(__uint_as_float(v[b][j2]));
+          __syncwarp();
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq) {  // 64 pieces of 8 n: (m = piece / 4, n = 8 * (piece % 4))
+            const int pc = lane + 32 * hq, j2 = pc >> 2, nn = 8 * (pc & 3);
+            const int m = m0 + c00 + 16 * b + j2, n = n0 + nn;
+            if (store && m < M && n < N)
+              *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[0]);  // the MMAs may refill the accumulator
+      if (lane == 0) mbar_arrive(&tempty_bar[ab]);  // the MMAs may refill the accumulator
     }
     if (!ok) atomicOr(&flags, 2);
   }
@@ -778,13 +786,22 @@ int sm_count_tc() {
 constexpr int kCounterBytes = 4096;
 constexpr int kMaxSplitTiles = kCounterBytes / 4;
 constexpr int kMaxSplits = 8;            // portable cluster size
-constexpr int kSmemLimit = 222 * 1024;   // opt-in dynamic shared memory of the kernel
+constexpr int kSmemLimit = 226 * 1024;   // opt-in dynamic shared memory of the kernel (+1 KB static)
 
 struct TcPlan {
-  int bm, stages, tmem_cols, splits, stages_per_split, tiles;
-  bool cluster, persist;
+  int bm, stages, tmem_cols, splits, stages_per_split, tiles, a_col0;
+  bool cluster, persist, dbl;
   size_t partial_bytes;
 };
+
+// Stages that fit both the shared memory (x ring and code slots) and the tensor memory left by
+// the accumulators.
+int fit_stages(int bm, bool dbl) {
+  const int acc = dbl ? 2 * bm : bm;
+  int st = 0;
+  while (st < kMaxStages && gemm_smem(bm, st + 1).epi_off <= kSmemBudget && acc + 64 * (st + 1) <= kTmemCols) ++st;
+  return st;
+}
 
 std::atomic<int> g_splitk_mode{W4A16_SPLITK_AUTO};
 
@@ -821,36 +838,44 @@ int max_clusters(int splits) {
 
 TcPlan plan_tc(int M, int N, int K) {
   TcPlan p;
-  p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
-  p.stages = 0;
-  while (p.stages < kMaxStages && gemm_smem(p.bm, p.stages + 1).total <= kSmemBudget) ++p.stages;
-  p.tmem_cols = kTmemCols;
-  p.tiles = ((N + kBN - 1) / kBN) * ((M + p.bm - 1) / p.bm);
+  const int ntn = (N + kBN - 1) / kBN;
   const int KS = num_ktiles(K);  // 128-k stages
+  const int sms = sm_count_tc();
+  p.bm = M >= 256 ? 256 : ((M + 15) / 16) * 16;
+  p.dbl = false;
+  p.tmem_cols = kTmemCols;
+  int tiles = ntn * ((M + p.bm - 1) / p.bm);
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
   // two 128-k stages per split and at most one cluster's worth of splits.  Where the device runs
   // clusters, all clusters of the launch must be resident at once (measured: a second wave of
   // clusters costs more than the splits gain), so the split count is lowered until they are;
   // both reductions use the same count, so they add the same partial tiles.
-  const int sms = sm_count_tc();
   const int mode = g_splitk_mode.load();
   const bool clusters = max_clusters(2) > 0;
   p.splits = 1;
-  if (4 * p.tiles < 3 * sms && p.tiles <= kMaxSplitTiles) {
-    p.splits = sms / p.tiles;
+  if (4 * tiles < 3 * sms && tiles <= kMaxSplitTiles) {
+    p.splits = sms / tiles;
     if (p.splits > KS / 2) p.splits = KS / 2;
     if (p.splits > kMaxSplits) p.splits = kMaxSplits;
     if (p.splits < 1) p.splits = 1;
     if (clusters)
-      while (p.splits > 1 && max_clusters(p.splits) < p.tiles) --p.splits;
+      while (p.splits > 1 && max_clusters(p.splits) < tiles) --p.splits;
   }
+  // Persistent CTAs (no split) alternate two accumulators when both fit in tensor memory beside
+  // the A stages (BM <= 160), so that a tile's drain overlaps the next tile's MMAs.  Larger M
+  // keeps BM = 256 and one accumulator: measured, one tcgen05.mma takes the issuing lane ~90
+  // cycles, so the 64-cycle MMAs of BM = 128 left the tensor pipe idle (gate_up M = 2048: 109 us
+  // against 84 us at BM = 256).
+  if (p.splits == 1) p.dbl = p.bm <= 160;
+  p.tiles = tiles;
+  p.stages = fit_stages(p.bm, p.dbl);
+  p.a_col0 = kTmemCols - 64 * p.stages;
   p.stages_per_split = (KS + p.splits - 1) / p.splits;
   p.splits = (KS + p.stages_per_split - 1) / p.stages_per_split;  // no empty split
   p.cluster = p.splits > 1 && mode != W4A16_SPLITK_GLOBAL && clusters && max_clusters(p.splits) >= p.tiles;
   p.partial_bytes = (p.splits > 1 && !p.cluster) ? (size_t)p.splits * p.tiles * p.bm * kBN * sizeof(float) : 0;
-  // Without a split, one CTA per SM walks the tiles and dedicated epilogue warps drain each
-  // finished accumulator while the producers run ahead on the next tile
   p.persist = p.splits == 1;
+  if (!p.persist) p.dbl = false;
   return p;
 }
 
@@ -893,6 +918,8 @@ cudaError_t launch_gemm_tc_t(const uint16_t *x, const void *packed, int M, int N
   sp.cluster = P.cluster ? 1 : 0;
   sp.stages_per_split = P.stages_per_split;
   sp.persist = P.persist ? 1 : 0;
+  sp.dbl = P.dbl ? 1 : 0;
+  sp.a_col0 = P.a_col0;
   sp.ntn = (N + kBN - 1) / kBN;
   sp.ntm = (M + P.bm - 1) / P.bm;
   const bool global = P.partial_bytes > 0;
