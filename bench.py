@@ -276,6 +276,7 @@ def run_ours(args, rank, world, local_rank):
     prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
     embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
     bf16_layer = run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank)
+    configs = run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src)
 
     gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
     traffic = None
@@ -297,11 +298,84 @@ def run_ours(args, rank, world, local_rank):
         "embed": embed,
         "awq_to_standard": convert,
         "bf16_layer": bf16_layer,
+        "configs": configs,
         "e2e": e2e,
         "gpu_launches": len(launches) * args.steps,
         "clocks": clk.summary(),
     }
     return result
+
+
+def run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src):
+    """Secondary: the decode shapes at M=16 (8 launches of a shape per graph, distinct weights),
+    the 2048x2048 layer at M=1, and the LM head (2048x131072) at M=1, 8 and 512 over two weight
+    copies (268 MB, more than L2)."""
+    def graph_time(calls, reps):
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        stream.synchronize()
+        with torch.cuda.graph(g2, stream=stream):
+            for c in calls:
+                c()
+        for _ in range(3):
+            g2.replay()
+
+        def rep():
+            with torch.cuda.stream(stream):
+                g2.replay()
+        return timed(rep, reps) / (reps * len(calls))
+
+    def gemm_call(x, p, M, N, K, y, ws=None):
+        return lambda: w4.gemm(x, p, M, N, K, G, y=y, workspace=ws, stream=stream)
+
+    out = {}
+    M = 16
+    m16 = {}
+    for si, (name, K, N) in enumerate(DECODE_SHAPES):
+        x = torch.from_numpy(inputs.make_x(M, K, seed=16)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        ms = graph_time([gemm_call(x, lin[si][3], M, N, K, y) for lin in layers], min(500, max(20, args.steps // 20)))
+        b = alg_bytes(M, K, N)
+        m16[name] = {"us_per_launch": round(ms * 1e3, 3), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    out["decode_shapes_M16"] = m16
+    K, N = inputs.SHAPES["square"]
+    sq = []
+    for i in range(16):
+        h = inputs.make_weights(K, N, G, seed=900 + i)
+        sq.append(w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                            torch.from_numpy(h["scales"]).to(dev), K, N, G, stream=stream))
+    x = torch.from_numpy(inputs.make_x(1, K, seed=17)).to(dev)
+    y = torch.empty((1, N), dtype=torch.float16, device=dev)
+    ms = graph_time([gemm_call(x, p, 1, N, K, y) for p in sq], min(500, max(20, args.steps // 20)))
+    b = alg_bytes(1, K, N)
+    out["square_2048_M1"] = {"us_per_launch": round(ms * 1e3, 3), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                             "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    del sq
+    K, N = inputs.SHAPES["lm_head"]
+    heads = []
+    for i in range(2):
+        h = inputs.make_weights(K, N, G, seed=950 + i)
+        heads.append(w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                               torch.from_numpy(h["scales"]).to(dev), K, N, G, stream=stream))
+        del h
+    lm = {}
+    for M in (1, 8, 512):
+        x = torch.from_numpy(inputs.make_x(M, K, seed=18)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        ws = torch.zeros(max(1, w4.workspace_bytes(M, N, K, G)), dtype=torch.uint8, device=dev)
+        ms = graph_time([gemm_call(x, p, M, N, K, y, ws) for p in heads] * 2, min(100, max(5, args.steps // 100)))
+        b, fl = alg_bytes(M, K, N), 2.0 * M * N * K
+        e = {"us_per_launch": round(ms * 1e3, 2), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+             "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
+        e["frac"] = round(e["gbs"] / hbm, 3) if M <= 8 else round(e["tflops"] / bf16, 3)
+        e["bound"] = "hbm" if M <= 8 else "tensor"
+        lm["M%d" % M] = e
+    out["lm_head_2048x131072"] = lm
+    out["peak_source"] = peak_src
+    return out
 
 
 def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
