@@ -171,6 +171,38 @@ def test_gemm_lm_head_sampled(M):
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
 
 
+@pytest.mark.parametrize("N,M,g", [(131072, 1, 64), (131072, 4, 128), (30000, 2, 128), (30000, 3, 32)])
+def test_gemm_streaming_decode_wide(N, M, g):
+    """Decode of very wide layers (K = 2048, more than 1824 row-tiles): resident CTAs walk pairs of
+    row-tiles, prefetching the next pair's weights.  Sampled outputs against the oracle, the last
+    columns (an odd row-tile count at N = 30000) included."""
+    K = 2048
+    L = Layer(K, N, g, seed=N + M)
+    x = inputs.make_x(M, K, seed=M)
+    y = L.gemm(x).float().cpu().numpy()
+    assert w4.last_device_error() == 0
+    rng = np.random.default_rng(N + g)
+    mi = rng.integers(0, M, 4096)
+    ni = np.concatenate([rng.integers(0, N, 4096 - 48), np.arange(N - 48, N)])
+    ref = oracle.linear_sampled(x.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, g, mi, ni)
+    ref16 = oracle.double_to_half_bits(ref).view(np.float16).astype(np.float64)
+    mx, mean = errors(y[mi, ni], ref16)
+    assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
+
+
+def test_streaming_decode_header_mismatch_writes_nothing():
+    K, N, g = 2048, 30000, 128
+    L = Layer(K, N, g, seed=5)
+    bad = L.packed.clone()
+    bad[0] ^= 0xFF
+    x = torch.from_numpy(inputs.make_x(1, K)).to(dev())
+    y = torch.full((1, N), 7.0, dtype=torch.float16, device=dev())
+    w4.gemm(x, bad, 1, N, K, g, y=y)
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    assert torch.all(y == 7.0)
+    assert w4.last_device_error() == 0
+
+
 @pytest.mark.parametrize("name,M,g", [("gate_up", 300, 128), ("gate_up", 1000, 64), ("lm_head", 200, 32),
                                      ("lm_head", 100, 128), ("lm_head", 150, 64), ("lm_head", 48, 32)])
 def test_gemm_persistent_ragged_sampled(name, M, g):

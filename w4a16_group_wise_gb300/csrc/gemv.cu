@@ -37,6 +37,8 @@
 // nibble conversion, the scale multiply, the mma.sync operand type and the output rounding).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "dq.cuh"
 #include "kernels.h"
 #include "layout.cuh"
@@ -245,6 +247,49 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 constexpr int kSmallRows = 4;   // rows of x per CTA in the lean variant
 constexpr int kSmallWarps = 8;
 
+// One chunk slot of a lean or streaming CTA: (q - z) * s * x of the lane's weights (RT row-tiles x
+// rows r8, r8 + 8 x its 32 k) into the MMA accumulators acc[RT][4]; xs: the lane's 32 k of x row
+// r8 in shared memory (zeros where xrow is false).
+template <class T, int RT, bool FACTOR>
+__device__ __forceinline__ void slot_mma(const uint4 (&code)[RT][2], const uint32_t (&scale)[RT],
+                                         const uint32_t (&zero)[RT], const uint8_t *xs, bool xrow,
+                                         float (&acc)[RT][4]) {
+#pragma unroll
+  for (int r = 0; r < RT; ++r) {
+    const ZeroBias zb0 = T::zb(zero[r] & 0xFu), zb1 = T::zb((zero[r] >> 4) & 0xFu);
+    float dd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint4 c0 = code[r][0], c1 = code[r][1];
+      const uint32_t w0 = (w == 0) ? c0.x : (w == 1) ? c0.y : (w == 2) ? c0.z : c0.w;
+      const uint32_t w1 = (w == 0) ? c1.x : (w == 1) ? c1.y : (w == 2) ? c1.z : c1.w;
+      uint32_t v0[4], v1[4];
+      T::qz(w0, zb0, v0);
+      T::qz(w1, zb1, v1);
+      if (!FACTOR) {
+        const uint32_t s20 = (scale[r] & 0xFFFFu) * 0x00010001u, s21 = (scale[r] >> 16) * 0x00010001u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v0[e] = T::mul2(v0[e], s20);
+          v1[e] = T::mul2(v1[e], s21);
+        }
+      }
+      const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
+      float *dst = FACTOR ? dd : acc[r];
+      T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+      T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+    }
+    if (FACTOR) {
+      const float f0 = T::to_float(scale[r] & 0xFFFFu);
+      const float f1 = T::to_float(scale[r] >> 16);
+      acc[r][0] = fmaf(f0, dd[0], acc[r][0]);
+      acc[r][1] = fmaf(f0, dd[1], acc[r][1]);
+      acc[r][2] = fmaf(f1, dd[2], acc[r][2]);
+      acc[r][3] = fmaf(f1, dd[3], acc[r][3]);
+    }
+  }
+}
+
 template <class T, int D, int RT, bool FACTOR>
 __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
@@ -317,42 +362,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
       if (j < mine) {
         cp_async_wait_pending<D - 1>();  // this slot's x has landed (for this lane's pieces)
         __syncwarp();                     // ... and every lane's pieces are visible
-        const uint8_t *xs = &xring[warp][d][r8 * 256 + 64 * t];
-        const bool xrow = r8 < M;
-#pragma unroll
-        for (int r = 0; r < RT; ++r) {
-          const ZeroBias zb0 = T::zb(zero[d][r] & 0xFu), zb1 = T::zb((zero[d][r] >> 4) & 0xFu);
-          float dd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint4 c0 = code[d][r][0], c1 = code[d][r][1];
-            const uint32_t w0 = (w == 0) ? c0.x : (w == 1) ? c0.y : (w == 2) ? c0.z : c0.w;
-            const uint32_t w1 = (w == 0) ? c1.x : (w == 1) ? c1.y : (w == 2) ? c1.z : c1.w;
-            uint32_t v0[4], v1[4];
-            T::qz(w0, zb0, v0);
-            T::qz(w1, zb1, v1);
-            if (!FACTOR) {
-              const uint32_t s20 = (scale[d][r] & 0xFFFFu) * 0x00010001u, s21 = (scale[d][r] >> 16) * 0x00010001u;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                v0[e] = T::mul2(v0[e], s20);
-                v1[e] = T::mul2(v1[e], s21);
-              }
-            }
-            const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
-            float *dst = FACTOR ? dd : acc[r];
-            T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
-            T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
-          }
-          if (FACTOR) {
-            const float f0 = T::to_float(scale[d][r] & 0xFFFFu);
-            const float f1 = T::to_float(scale[d][r] >> 16);
-            acc[r][0] = fmaf(f0, dd[0], acc[r][0]);
-            acc[r][1] = fmaf(f0, dd[1], acc[r][1]);
-            acc[r][2] = fmaf(f1, dd[2], acc[r][2]);
-            acc[r][3] = fmaf(f1, dd[3], acc[r][3]);
-          }
-        }
+        slot_mma<T, RT, FACTOR>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], r8 < M, acc);
         __syncwarp();  // every lane is done reading the slot before it is refilled
         if (j + D < mine) {
           load_w(d, j + D);
@@ -385,6 +395,107 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
   }
 }
 
+
+// ---------------------------------------------------------------------------------------------
+// Streaming variant for very wide layers with K <= 2048 (at most two chunks per warp), where the
+// lean kernel would need more than two waves of CTAs (the tied LM head: 8192 row-tiles).  Three
+// CTAs per SM stay resident and walk pairs of row-tiles u = blockIdx.x, + gridDim.x, ...; x is
+// fetched once into shared memory; a warp requests its weights of the next pair as soon as those
+// of the current pair are in registers, so the weight stream does not wait for a CTA to exit and
+// a new one to start.  The packed header is checked before any weight is read.
+template <class T, bool FACTOR>
+__global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
+    const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
+    int units, uint16_t *__restrict__ y, int *err) {
+  constexpr int RT = 2, D = 2;
+  __shared__ __align__(16) uint8_t xring[kSmallWarps][D][kSmallRows * 256];
+  __shared__ float red[kSmallWarps][RT * 4][32];
+  __shared__ int bad;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r8 = lane >> 2, t = lane & 3;
+  const int CB = chunk_bytes(g);
+  const int mine = (KT - warp + kSmallWarps - 1) / kSmallWarps;  // chunks warp, warp + 8 (KT <= 16)
+
+  if (threadIdx.x == 0) {
+    const Header *h = reinterpret_cast<const Header *>(packed);
+    bad = !((h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
+            (h->dtype == T::kDtype));
+    if (bad && blockIdx.x == 0) atomicOr(err, 1);
+  }
+  __syncthreads();
+  if (bad) return;
+
+  uint4 code[D][RT][2];
+  uint32_t scale[D][RT], zero[D][RT];
+  auto load_w = [&](int d, int u) {  // chunk warp + 8 d of row-tile pair u
+    const int tile0 = u * RT, b = tile0 / 4, i0 = tile0 % 4;
+    const uint8_t *ch = packed + kHeaderBytes + ((size_t)b * KT + warp + d * kSmallWarps) * CB;
+    const uint8_t *meta = ch + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const int i = i0 + r;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) code[d][r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
+      scale[d][r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
+      zero[d][r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+    }
+  };
+
+  int u = blockIdx.x;
+#pragma unroll
+  for (int d = 0; d < D; ++d)
+    if (d < mine) load_w(d, u);
+  griddep_launch_dependents();
+  griddep_wait();  // x may be the previous kernel's output; y may still be read by it
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    if (d < mine) {
+      const int k0 = (warp + d * kSmallWarps) * kTileK;
+      for (int pp = lane; pp < M * 16; pp += 32) {
+        const int m = pp / 16, q = pp % 16;
+        const bool ok = k0 + 8 * q < K;
+        cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
+      }
+    }
+  }
+  cp_async_commit();
+  cp_async_wait_pending<0>();
+  __syncwarp();
+
+  for (; u < units; u += gridDim.x) {
+    float acc[RT][4];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+    const int un = u + (int)gridDim.x;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (d < mine) {
+        slot_mma<T, RT, FACTOR>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], r8 < M, acc);
+        if (un < units) load_w(d, un);  // the next pair's weights stream in meanwhile
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) red[warp][4 * r + c][lane] = acc[r][c];
+    __syncthreads();
+    if (threadIdx.x < RT * 128) {
+      const int ln = threadIdx.x % 32, c = (threadIdx.x / 32) % 4, r = threadIdx.x / 128;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSmallWarps; ++w) v += red[w][4 * r + c][ln];
+      const int tile0 = u * RT, b = tile0 / 4, i0 = tile0 % 4;
+      const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
+      const int m = 2 * (ln & 3) + (c & 1);
+      const int n = b * kBlockN + row;
+      if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
+    }
+    __syncthreads();  // red is rewritten by the next pair
+  }
+}
 
 int sm_count() {
   static int count[64];
@@ -435,6 +546,24 @@ cudaError_t launch_rt(int tiles, int mblocks, int W, int MB, bool factor, const 
                 : launch_variant<T, RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
 }
 
+template <class T>
+cudaError_t launch_stream(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
+                          int KT, uint16_t *y, int *err, cudaStream_t stream) {
+  const int units = (tiles + 1) / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(units, 3 * sm_count()));
+  cfg.blockDim = dim3(32 * kSmallWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, true>, x, p, M, N, K, g, KT, units, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, false>, x, p, M, N, K, g, KT, units, y, err);
+}
+
 template <class T, int D, int RT>
 cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
                          int KT, uint16_t *y, int *err, cudaStream_t stream) {
@@ -467,8 +596,11 @@ cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, i
   const bool long_k = KT >= 32 && ctas1 <= sm_count();
   if (M <= kSmallRows && !long_k) {
     // one-tile CTAs (4 per SM) while they fit in one wave; two-tile CTAs (3 per SM) beyond, so
-    // that every CTA is resident and has issued all its weight loads when the wait ends
+    // that every CTA is resident and has issued all its weight loads when the wait ends; resident
+    // streaming CTAs where two-tile CTAs would need more than two waves (K <= 2048)
     if (ctas1 <= 4L * sm_count()) return launch_small<T, 2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+    if (KT <= 2 * kSmallWarps && ctas1 > 12L * sm_count())
+      return launch_stream<T>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
     return launch_small<T, 2, 2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
   }
   // Two row-tiles per CTA once the grid would cover the GPU several times over (a 2-tile CTA
