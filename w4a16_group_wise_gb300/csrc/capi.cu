@@ -222,11 +222,15 @@ const char *w4a16_status_string(int status) {
   switch (status) {
     case W4A16_OK: return "ok";
     case W4A16_ERR_INVALID: return "invalid argument (null pointer, non-positive size or bad n-range)";
-    case W4A16_ERR_UNSUPPORTED: return "unsupported shape (need N % 8 == 0, K % g == 0, g in {32, 64, 128})";
+    case W4A16_ERR_UNSUPPORTED:
+      return "unsupported shape (need N % 8 == 0 and g in {32, 64, 128} with K % g == 0, or g == K or -1 with "
+             "K % 32 == 0)";
     case W4A16_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
     case W4A16_ERR_WORKSPACE: return "workspace smaller than w4a16_workspace_bytes";
     case W4A16_ERR_CUDA: return "CUDA call or kernel launch failed";
-    case W4A16_ERR_DEVICE: return "device-side error (packed header mismatch or wait timeout)";
+    case W4A16_ERR_DEVICE:
+      return "device-side error (packed buffer of another shape or element type, token id out of range, or a "
+             "wait that timed out)";
     default: return "unknown status";
   }
 }

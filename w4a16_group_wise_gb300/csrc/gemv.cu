@@ -1,5 +1,10 @@
 // gemv.cu -- decode path of y = x . W for few rows of x (up to 16 per m-block).
 //
+// Three kernels, picked by launch_gemv from M, K and the number of 16-column row-tiles:
+// gemv_kernel (any M, x in registers), gemv_small_kernel (M <= 4, x through a per-warp cp.async
+// ring, 64-80 registers so that 3-4 CTAs fit per SM) and gemv_stream_kernel (M <= 4, K <= 2048
+// and very wide layers: resident CTAs walking row-tile pairs).  What follows holds for all three.
+//
 // Why a separate path: "single-stream decode reads every weight to emit one token, so bits
 // per weight set the token rate" (vllm-omni commit "Add cpu_int4, an asymmetric 4-bit weight
 // path for vLLM's CPU backend").  The kernel streams the packed weights exactly once, with
