@@ -218,6 +218,16 @@ int w4a16_dequant_bf16(const void *packed, int K, int N, int g, uint16_t *W, voi
 int w4a16_embed_bf16(const int32_t *ids, int T, const void *packed, int K, int N, int g, uint16_t *out,
                      void *stream);
 
+/* Self-test of failure detection, faulting nothing: one thread waits, with the library's bounded
+ * waits (polling, then sleeping), on a barrier that never completes, each giving up after
+ * limit_ns nanoseconds (0 < limit_ns <= 100 ms).  *status (a 4-byte aligned device int) gets
+ * bit 0 if the polling wait gave up and bit 1 if the sleeping one did (3 when both work), and
+ * the device error word records the timeout as the GEMM kernels do: w4a16_last_device_error then
+ * returns W4A16_ERR_DEVICE, and the context stays usable.  The analogue of the pages' benchmark
+ * harness that records failures instead of dropping them (vllm-omni commit "cpu_int4:
+ * dequantize prefill weights from the tinygemm layout, not a copy"). */
+int w4a16_selftest_wait_timeout(int64_t limit_ns, int *status, void *stream);
+
 /* Static description of a status code. */
 const char *w4a16_status_string(int status);
 

@@ -177,3 +177,12 @@ def test_bf16_inputs_are_rounded_draws():
     assert np.array_equal(h["qweight"], hf["qweight"]) and np.array_equal(h["qzeros"], hf["qzeros"])
     s = (h["scales"].astype(np.uint32) << 16).view(np.float32)
     assert np.all((s >= 0.002 * (1 - 2 ** -8)) & (s <= 0.02 * (1 + 2 ** -8)))
+
+
+def test_selftest_wait_timeout_host_validation(L):
+    # rejected before any launch (the pointer is never dereferenced)
+    assert L.w4a16_selftest_wait_timeout(0, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_selftest_wait_timeout(-5, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_selftest_wait_timeout(200_000_000, P, NUL) == binding.ERR_INVALID
+    assert L.w4a16_selftest_wait_timeout(1_000_000, NUL, NUL) == binding.ERR_INVALID
+    assert L.w4a16_selftest_wait_timeout(1_000_000, ctypes.c_void_p(0x10002), NUL) == binding.ERR_MISALIGNED

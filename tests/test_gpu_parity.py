@@ -327,6 +327,22 @@ def test_header_mismatch_is_reported_and_nothing_written():
     assert_close(y_ok, y16)
 
 
+def test_bounded_waits_time_out_and_the_context_stays_usable():
+    """Failure detection without a fault: the library's bounded waits, on a barrier that never
+    completes, give up after the limit and record the timeout; the context keeps working."""
+    assert w4.last_device_error() == 0
+    assert w4.binding.selftest_wait_timeout(1_000_000) == 3   # both the polling and the sleeping wait
+    assert w4.last_device_error() == w4.binding.ERR_DEVICE
+    assert w4.last_device_error() == 0                        # the record is cleared
+    K, N, g = 512, 128, 128
+    L = Layer(K, N, g, seed=40)
+    for M in (3, 64):
+        x = inputs.make_x(M, K, seed=M)
+        _, y16 = L.ref(x)
+        assert_close(L.gemm(x), y16)
+    assert w4.last_device_error() == 0
+
+
 def test_nondefault_stream():
     K, N, g = 2048, 3072, 128
     L = Layer(K, N, g, seed=14)

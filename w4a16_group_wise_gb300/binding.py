@@ -41,6 +41,7 @@ SIGNATURES = {
     "w4a16_set_option": ([_I, _I], _I),
     "w4a16_embed": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
     "w4a16_awq_to_standard": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "w4a16_selftest_wait_timeout": ([_I64, _P, _P], _I),
     "w4a16_repack_bf16": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "w4a16_repack_chunk_bf16": ([_P, _I64, _P, _I64, _P, _I64, _I, _I, _I, _I, _I, _P, _P], _I),
     "w4a16_gemm_bf16": ([_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
@@ -228,6 +229,15 @@ def awq_to_standard(qweight, qzeros, K, N, g, stream=None):
     _check("w4a16_awq_to_standard", lib().w4a16_awq_to_standard(_ptr(qweight), _ptr(qzeros), K, N, g, _ptr(qs),
                                                                  _ptr(zs), _stream(stream)))
     return qs, zs
+
+
+def selftest_wait_timeout(limit_ns=1_000_000, stream=None):
+    """Forced timeout of the library's bounded waits (see include/w4a16.h): returns the bitmask of
+    waits that gave up (3 when both did); the device error word then reports W4A16_ERR_DEVICE."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check("w4a16_selftest_wait_timeout", lib().w4a16_selftest_wait_timeout(int(limit_ns), _ptr(status),
+                                                                           _stream(stream)))
+    return int(status.item())
 
 
 def last_device_error(stream=None):

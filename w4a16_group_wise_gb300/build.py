@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "_libw4a16.so")
-SOURCES = ["capi.cu", "repack.cu", "dequant.cu", "gemv.cu", "gemm_tc.cu", "noalloc.cu", "embed.cu", "convert.cu"]
+SOURCES = ["capi.cu", "repack.cu", "dequant.cu", "gemv.cu", "gemm_tc.cu", "noalloc.cu", "embed.cu", "convert.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

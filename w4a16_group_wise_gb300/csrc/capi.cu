@@ -255,6 +255,14 @@ int w4a16_last_device_error(void *stream) {
 
 int w4a16_layout_version(void) { return (int)kLayoutVersion; }
 
+int w4a16_selftest_wait_timeout(int64_t limit_ns, int *status, void *stream) {
+  if (limit_ns <= 0 || limit_ns > 100000000 || !status) return W4A16_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(status) & 3u) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_wait_timeout((uint64_t)limit_ns, status, err, static_cast<cudaStream_t>(stream)));
+}
+
 int w4a16_set_option(int option, int value) {
   if (option == W4A16_OPT_SPLITK_REDUCTION) return set_splitk_mode(value);
   return W4A16_ERR_INVALID;

@@ -47,6 +47,10 @@ cudaError_t launch_awq_to_standard(const int32_t *qweight_awq, const int32_t *qz
                                    int zero_rows, int32_t *qweight_std, int32_t *qzeros_std,
                                    cudaStream_t stream);
 
+// Forced timeout of the bounded waits: one thread waits (polling, then sleeping) on an mbarrier
+// that nothing arrives at, with the given limit; *status gets a bit per wait that gave up.
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int *status, int *err, cudaStream_t stream);
+
 // The packed layout's group size for a caller's g (32, 64 or 128; or one group over all of K,
 // g == K or g == -1, stored as the largest of 128, 64, 32 dividing K); 0 when unsupported.
 int layout_group(int K, int g);
