@@ -135,6 +135,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def nvtx_range(name):
+    """An NVTX range around a bench block, for profiler timelines; a no-op where torch has no NVTX."""
+    import contextlib
+    import torch
+    try:
+        torch.cuda.nvtx.range_push(name)
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        return contextlib.nullcontext()
+    return torch.cuda.nvtx.range(name)
+
+
 def source_sha(path):
     """sha256 of a source file's code: // comments and blank lines removed, so that a comment-only
     edit does not invalidate numbers taken from the compiled kernel."""
@@ -211,7 +223,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             graph.replay()
 
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank) as clk, nvtx_range("decode step (timed)"):
         ms = timed(replay, args.steps)
     ms_step = ms / args.steps
     value = whole_job_rate(step_bytes, world, ms_step) / 1e9
@@ -271,16 +283,21 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         e2e_step()
-    ms_e2e = timed(e2e_step, args.steps) / args.steps
+    with nvtx_range("e2e (host copies + C-ABI calls)"):
+        ms_e2e = timed(e2e_step, args.steps) / args.steps
     e2e = {"value": round(whole_job_rate(step_bytes, world, ms_e2e) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
            "ms_per_step": round(ms_e2e, 4)}
 
     # ---------------- prefill M=512 (secondary): TFLOP/s of the three shapes
-    prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
-    embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
-    bf16_layer = run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank)
-    configs = run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src)
+    with nvtx_range("prefill M=512"):
+        prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
+    with nvtx_range("embed gather and AWQ conversion"):
+        embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
+    with nvtx_range("bf16 layer"):
+        bf16_layer = run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank)
+    with nvtx_range("other configurations"):
+        configs = run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src)
 
     gemv_src = os.path.join(ROOT, "w4a16_group_wise_gb300", "csrc", "gemv.cu")
     traffic = None
