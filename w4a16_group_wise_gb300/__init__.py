@@ -6,4 +6,5 @@ The compute is a C-ABI CUDA library (include/w4a16.h, csrc/); ``binding`` marsha
 tensors into it.  ``inputs`` draws the seeded synthetic tensors used by tests and benchmarks.
 """
 from .binding import (W4A16Error, awq_to_standard, dequant, embed, gemm, gemm_noalloc, last_device_error, layout_version,  # noqa: F401
-                      packed_bytes, repack, repack_chunk, set_option, status_string, workspace_bytes)
+                      packed_bytes, repack, repack_chunk, selftest_wait_timeout, set_option, status_string,
+                      workspace_bytes)
