@@ -171,12 +171,13 @@ def test_gemm_lm_head_sampled(M):
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
 
 
-@pytest.mark.parametrize("N,M,g", [(131072, 1, 64), (131072, 4, 128), (30000, 2, 128), (30000, 3, 32)])
-def test_gemm_streaming_decode_wide(N, M, g):
-    """Decode of very wide layers (K = 2048, more than 1824 row-tiles): resident CTAs walk pairs of
-    row-tiles, prefetching the next pair's weights.  Sampled outputs against the oracle, the last
-    columns (an odd row-tile count at N = 30000) included."""
-    K = 2048
+@pytest.mark.parametrize("N,K,M,g", [(131072, 2048, 1, 64), (131072, 2048, 4, 128), (30000, 2048, 2, 128),
+                                     (30000, 2048, 3, 32), (30000, 320, 1, 64), (40000, 128, 2, 128)])
+def test_gemm_streaming_decode_wide(N, K, M, g):
+    """Decode of very wide layers (K <= 2048, more than 1824 row-tiles): resident CTAs walk pairs
+    of row-tiles, prefetching the next pair's weights.  Sampled outputs against the oracle, the
+    last columns (an odd row-tile count at N = 30000) included; at K = 320 and 128 most warps have
+    no chunk, and K = 320 ends in a half-filled chunk."""
     L = Layer(K, N, g, seed=N + M)
     x = inputs.make_x(M, K, seed=M)
     y = L.gemm(x).float().cpu().numpy()
