@@ -41,7 +41,7 @@ METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate
 # captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch each of q_k_v, gate_up
 # and down at M=1, summarised under profiles/), keyed by the sha256 of the kernel source they
 # were taken on; reported as null whenever that source has changed since.
-TRAFFIC = {"source_sha256": "1e4b7099fd71b46cc1f84ed419d7d176a7339c10762084c91a9899e0ee2b1b84",
+TRAFFIC = {"source_sha256": "5226c4f59f644360a379b12cb7716502a93256257849bddd969bec8d55116b71",
            "bytes_per_launch": (3299328 + 14200576 + 7120128) // 3}
 
 

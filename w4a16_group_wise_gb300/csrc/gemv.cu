@@ -1,8 +1,8 @@
 // gemv.cu -- decode path of y = x . W for few rows of x (up to 16 per m-block).
 //
 // Three kernels, picked by launch_gemv from M, K and the number of 16-column row-tiles:
-// gemv_kernel (any M, x in registers), gemv_small_kernel (M <= 4, x through a per-warp cp.async
-// ring, 64-80 registers so that 3-4 CTAs fit per SM) and gemv_stream_kernel (M <= 4, K <= 2048
+// gemv_kernel (any M, x in registers), gemv_small_kernel (M <= 8, x through a per-warp cp.async
+// ring, 64-80 registers so that 3-4 CTAs fit per SM) and gemv_stream_kernel (M <= 8, K <= 2048
 // and very wide layers: resident CTAs walking row-tile pairs).  What follows holds for all three.
 //
 // Why a separate path: "single-stream decode reads every weight to emit one token, so bits
@@ -244,12 +244,12 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 
 
 // ---------------------------------------------------------------------------------------------
-// Lean variant for M <= 4 (the decode case): a warp streams its x slices into a private
+// Lean variant for M <= 8 (the decode case): a warp streams its x slices into a private
 // shared-memory ring with cp.async, issued together with the weights D chunks ahead, so x costs
 // no registers and the kernel fits in <= 64 registers per thread -- four 8-warp CTAs per SM.
 // HBM throughput of plain loads follows the number of warps with loads outstanding more than
 // the bytes each has in flight, so this is what lets the decode stream reach the bandwidth.
-constexpr int kSmallRows = 4;   // rows of x per CTA in the lean variant
+constexpr int kSmallRows = 8;   // rows of x per CTA in the lean variant: the 8 columns of the MMA's B
 constexpr int kSmallWarps = 8;
 
 // One chunk slot of a lean or streaming CTA: (q - z) * s * x of the lane's weights (RT row-tiles x
@@ -299,7 +299,7 @@ template <class T, int D, int RT, bool FACTOR>
 __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
     uint16_t *__restrict__ y, int *err) {
-  // x ring: [warp][D slots][kSmallRows rows][128 k] fp16 = 1 KB per slot
+  // x ring: [warp][D slots][kSmallRows rows][128 k] fp16 = 2 KB per slot
   __shared__ __align__(16) uint8_t xring[kSmallWarps][D][kSmallRows * 256];
   __shared__ float red[kSmallWarps][RT * 4][32];
   __shared__ int bad;
@@ -597,7 +597,7 @@ cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, i
   const uint8_t *p = static_cast<const uint8_t *>(packed);
   const bool factor = (g == kTileK);
   const long ctas1 = (long)tiles * mblocks;
-  // Lean variant for M <= 4 unless K is long and the grid is small (then 16 warps per CTA win).
+  // Lean variant for M <= 8 unless K is long and the grid is small (then 16 warps per CTA win).
   const bool long_k = KT >= 32 && ctas1 <= sm_count();
   if (M <= kSmallRows && !long_k) {
     // one-tile CTAs (4 per SM) while they fit in one wave; two-tile CTAs (3 per SM) beyond, so
