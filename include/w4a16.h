@@ -178,10 +178,14 @@ int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq,
  * exists only for such callers).  The caller still provides x, packed and y as for
  * w4a16_gemm.  Returns W4A16_ERR_WORKSPACE when the problem's scratch (w4a16_workspace_bytes)
  * exceeds that size.  All calls share the one array, so calls that overlap on the GPU race with
- * each other and must be serialized.  The first call on a device sets that device up
- * (looks up the array and clears the counters at its head, synchronously), so make it before
- * capturing the stream; every completed call leaves those counters cleared again.  Never calls
- * cudaMalloc, cudaFree or any other allocating routine. */
+ * each other and must be serialized.  The first call on a device sets that device up (looks up
+ * the array and clears the counters at its head, ordered on `stream` before the call's kernel),
+ * so make it before capturing the stream; every completed call leaves those counters cleared
+ * again.  Never calls cudaMalloc, cudaFree or any other allocating routine.  The array's device
+ * memory is not free, though: CUDA commits the library's device code and this array on a device
+ * when the library is first used there, which can be inside the first call, and that call then
+ * fails with W4A16_ERR_CUDA if the device is out of memory; a caller that must not fail later
+ * makes one call (or any other call of this library) on each device at start-up. */
 int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                        void *stream);
 

@@ -171,6 +171,23 @@ def test_gemm_lm_head_sampled(M):
     assert mx <= 2e-2 and mean <= 5e-3, (mx, mean)
 
 
+@pytest.mark.parametrize("K,N,M,g", [(2048, 7304, 1, 128), (2048, 19456, 5, 128), (4096, 7304, 8, 64),
+                                     (11008, 512, 2, 128), (1024, 2440, 7, 32), (2048, 13312, 6, 128)])
+def test_gemm_decode_shapes_between_the_layers(K, N, M, g):
+    """Decode (M <= 8) at shapes between and around the decoder layers: a last row-tile with 8
+    columns (N = 7304, 2440), a grid of row-tile pairs (N = 19456), a long K (86 chunks), several
+    rows of x, groups of 32, 64 and 128.  Every output against the oracle, twice (the same bits
+    both times)."""
+    L = Layer(K, N, g, seed=K + N + M)
+    x = inputs.make_x(M, K, seed=M)
+    _, y16 = L.ref(x)
+    a = L.gemm(x)
+    assert_close(a, y16)
+    b = L.gemm(x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert w4.last_device_error() == 0
+
+
 @pytest.mark.parametrize("N,K,M,g", [(131072, 2048, 1, 64), (131072, 2048, 4, 128), (30000, 2048, 2, 128),
                                      (30000, 2048, 3, 32), (30000, 320, 1, 64), (40000, 128, 2, 128)])
 def test_gemm_streaming_decode_wide(N, K, M, g):

@@ -1,17 +1,18 @@
-"""w4a16_gemm_noalloc against w4a16_gemm, through the C ABI.
+"""w4a16_gemm_noalloc through the C ABI, against the oracle and against w4a16_gemm.
 
 w4a16_gemm_noalloc serves callers that cannot allocate device memory (a runtime that plans every
 buffer ahead, a host that forbids allocation after start-up, a latency-critical path): where the
 tensor-core path adds split-K partial tiles through memory, it keeps them in an array built into
-the library instead of a caller workspace.  That array is shared by every call and keeps the previous call's contents, so the
-results are checked on two calls in a row, against the ordinary entry point, within the same
-tolerance as the other GEMM tests.  This file is collected last on purpose.
+the library instead of a caller workspace.  That array is shared by every call and keeps the
+previous call's contents, so the results are checked on two calls in a row, each element against
+the CPU oracle within the tolerance of the other GEMM tests, and against the ordinary entry point.
+This file is collected last on purpose.
 """
 import ctypes
 
 import pytest
 
-from gpu_util import MAX_TOL, MEAN_TOL, Layer, dev, errors, torch
+from gpu_util import MAX_TOL, MEAN_TOL, Layer, assert_close, dev, errors, torch
 import w4a16_group_wise_gb300 as w4
 from w4a16_group_wise_gb300 import binding, inputs
 
@@ -26,6 +27,20 @@ def _call(x, packed, M, N, K, g, y):
 # split-K shapes (scratch in use), a shape that needs none, the decode path, the N = 80 tail
 CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 512, 128), ("square", 40, 128),
          ("gate_up", 512, 128), ("gate_up", 1, 128), ("tail80", 17, 32)]
+# the cases that split K: under the workspace reduction they run through the built-in scratch
+SPLIT = {("down", 512), ("qkv", 129), ("qkv", 512), ("square", 40)}
+
+_refs = {}
+
+
+def _layer_and_ref(name, M, g):
+    """The seeded layer, x, and the oracle's fp16 y of a case (computed once per case)."""
+    if (name, M, g) not in _refs:
+        K, N = inputs.SHAPES[name]
+        L = Layer(K, N, g, seed=21)
+        x = inputs.make_x(M, K, seed=21)
+        _refs[(name, M, g)] = (L, x, L.ref(x)[1])
+    return _refs[(name, M, g)]
 
 
 @pytest.mark.gpu
@@ -37,15 +52,19 @@ def test_noalloc_matches_workspace_entry_point(name, M, g, reduction):
     w4.set_option(binding.OPT_SPLITK_REDUCTION, reduction)
     try:
         K, N = inputs.SHAPES[name]
-        L = Layer(K, N, g, seed=21)
-        x = torch.from_numpy(inputs.make_x(M, K, seed=21)).to(dev())
-        ref = w4.gemm(x, L.packed, M, N, K, g).float().cpu().numpy()
-        assert w4.workspace_bytes(M, N, K, g) <= 24 << 20  # within the built-in scratch
+        L, x_np, y16 = _layer_and_ref(name, M, g)
+        x = torch.from_numpy(x_np).to(dev())
+        need = w4.workspace_bytes(M, N, K, g)
+        assert need <= 24 << 20  # within the built-in scratch
+        if reduction == binding.SPLITK_GLOBAL and (name, M) in SPLIT:
+            assert need > 0  # the case does go through the scratch
+        ws_ref = w4.gemm(x, L.packed, M, N, K, g).float().cpu().numpy()
         for _ in range(2):
             y = torch.full((M, N), 3.0, dtype=torch.float16, device=dev())
             assert _call(x, L.packed, M, N, K, g, y) == binding.OK
             assert w4.last_device_error() == binding.OK
-            mx, mean = errors(y.float().cpu().numpy(), ref)
+            assert_close(y, y16)  # every element against the oracle
+            mx, mean = errors(y.float().cpu().numpy(), ws_ref)
             assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
     finally:
         w4.set_option(binding.OPT_SPLITK_REDUCTION, binding.SPLITK_AUTO)

@@ -101,7 +101,13 @@ int gemm_impl(const uint16_t *x, const void *packed, int M, int N, int K, int g,
   if (M == 0) return W4A16_OK;
   if (!x || !packed || !y) return W4A16_ERR_INVALID;
   if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
-  size_t need = M <= kDecodeMaxM ? 0 : gemm_tc_workspace_bytes(M, N, K);
+  // one plan per call: the workspace is checked against the plan that is launched
+  TcPlan plan = {};
+  size_t need = 0;
+  if (M > kDecodeMaxM) {
+    plan = plan_gemm_tc(M, N, K);
+    need = gemm_tc_workspace_bytes(plan);
+  }
   if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
   if (need > 0 && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
   int *err = device_error_word();
@@ -109,7 +115,7 @@ int gemm_impl(const uint16_t *x, const void *packed, int M, int N, int K, int g,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int gl = layout_group(K, g);
   if (M <= kDecodeMaxM) return map_launch(launch_gemv(x, packed, M, N, K, gl, dtype, y, err, s));
-  return map_launch(launch_gemm_tc(x, packed, M, N, K, gl, dtype, y, err, workspace, s));
+  return map_launch(launch_gemm_tc(plan, x, packed, M, N, K, gl, dtype, y, err, need > 0 ? workspace : nullptr, s));
 }
 
 int embed_impl(const int32_t *ids, int T, const void *packed, int K, int N, int g, int dtype, uint16_t *out,
@@ -150,7 +156,7 @@ size_t w4a16_packed_bytes(int K, int N, int g) {
 size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
   if (M < 0 || check_shape(K, N, g) != W4A16_OK) return 0;
   if (M <= kDecodeMaxM) return 0;
-  return gemm_tc_workspace_bytes(M, N, K);
+  return gemm_tc_workspace_bytes(plan_gemm_tc(M, N, K));
 }
 
 int w4a16_repack_chunk(const int32_t *qweight_c, int64_t ld_qweight, const int32_t *qzeros_c,

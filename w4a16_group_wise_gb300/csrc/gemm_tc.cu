@@ -773,7 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
 // --------------------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -785,6 +787,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
+
+namespace {
 
 int sm_count_tc() {
   static int count[64];
@@ -802,16 +806,10 @@ int sm_count_tc() {
 // Workspace of a split-K launch with the workspace reduction: kCounterBytes of per-tile
 // arrival counters at offset 0 (zero before the first call, left zero by every completed call,
 // whatever the shape), then the fp32 partial tiles (no initialisation needed).
-constexpr int kCounterBytes = 4096;
+constexpr int kCounterBytes = (int)kSplitCounterBytes;
 constexpr int kMaxSplitTiles = kCounterBytes / 4;
 constexpr int kMaxSplits = 8;            // portable cluster size
 constexpr int kSmemLimit = 226 * 1024;   // opt-in dynamic shared memory of the kernel (+1 KB static)
-
-struct TcPlan {
-  int bm, stages, tmem_cols, splits, stages_per_split, tiles, a_col0;
-  bool cluster, persist, dbl;
-  size_t partial_bytes;
-};
 
 // Stages that fit both the shared memory (x ring and code slots) and the tensor memory left by
 // the accumulators.
@@ -855,7 +853,9 @@ int max_clusters(int splits) {
   return cache[dev][splits] > 0 ? cache[dev][splits] : 0;
 }
 
-TcPlan plan_tc(int M, int N, int K) {
+}  // namespace
+
+TcPlan plan_gemm_tc(int M, int N, int K) {
   TcPlan p;
   const int ntn = (N + kBN - 1) / kBN;
   const int KS = num_ktiles(K);  // 128-k stages
@@ -898,12 +898,7 @@ TcPlan plan_tc(int M, int N, int K) {
   return p;
 }
 
-}  // namespace
-
-size_t gemm_tc_workspace_bytes(int M, int N, int K) {
-  const TcPlan p = plan_tc(M, N, K);
-  return p.partial_bytes ? kCounterBytes + p.partial_bytes : 0;
-}
+size_t gemm_tc_workspace_bytes(const TcPlan &p) { return p.partial_bytes ? kCounterBytes + p.partial_bytes : 0; }
 
 int set_splitk_mode(int mode) {
   if (mode != W4A16_SPLITK_AUTO && mode != W4A16_SPLITK_GLOBAL) return W4A16_ERR_INVALID;
@@ -914,12 +909,11 @@ int set_splitk_mode(int mode) {
 namespace {
 
 template <class T>
-cudaError_t launch_gemm_tc_t(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y, int *err,
-                             void *workspace, cudaStream_t stream) {
-  const TcPlan P = plan_tc(M, N, K);
+cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *packed, int M, int N, int K, int g,
+                             uint16_t *y, int *err, void *workspace, cudaStream_t stream) {
   const GemmSmem L = gemm_smem(P.bm, P.stages);
 
-  auto enc = encode_fn();
+  auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -977,10 +971,11 @@ cudaError_t launch_gemm_tc_t(const uint16_t *x, const void *packed, int M, int N
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype, uint16_t *y,
-                           int *err, void *workspace, cudaStream_t stream) {
-  return dtype == kDtypeBf16 ? launch_gemm_tc_t<Bf16>(x, packed, M, N, K, g, y, err, workspace, stream)
-                             : launch_gemm_tc_t<Fp16>(x, packed, M, N, K, g, y, err, workspace, stream);
+cudaError_t launch_gemm_tc(const TcPlan &plan, const uint16_t *x, const void *packed, int M, int N, int K, int g,
+                           int dtype, uint16_t *y, int *err, void *workspace, cudaStream_t stream) {
+  if (plan.partial_bytes > 0 && !workspace) return cudaErrorInvalidValue;
+  return dtype == kDtypeBf16 ? launch_gemm_tc_t<Bf16>(plan, x, packed, M, N, K, g, y, err, workspace, stream)
+                             : launch_gemm_tc_t<Fp16>(plan, x, packed, M, N, K, g, y, err, workspace, stream);
 }
 
 }  // namespace w4a16

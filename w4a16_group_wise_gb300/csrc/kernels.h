@@ -4,7 +4,9 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 namespace w4a16 {
 
@@ -28,14 +30,27 @@ cudaError_t launch_dequant(const void *packed, int K, int N, int g, int dtype, u
 cudaError_t launch_gemv(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype,
                         uint16_t *y, int *err, cudaStream_t stream);
 
-// Tensor-core path (tcgen05): y = x . W for M > kDecodeMaxM.  `workspace` holds
-// gemm_tc_workspace_bytes(M, N, K) bytes (may be null when that is 0); its counters must be zero
-// before the first call and are left zero by every completed call.
-cudaError_t launch_gemm_tc(const uint16_t *x, const void *packed, int M, int N, int K, int g, int dtype,
-                           uint16_t *y, int *err, void *workspace, cudaStream_t stream);
-size_t gemm_tc_workspace_bytes(int M, int N, int K);
+// Tensor-core path (tcgen05): y = x . W for M > kDecodeMaxM.  A call plans its launch once
+// (plan_gemm_tc, which reads the split-K reduction mode once), checks the workspace against that
+// plan's gemm_tc_workspace_bytes, and launches exactly that plan, so the scratch the kernel uses
+// is the scratch that was checked.  `workspace` holds gemm_tc_workspace_bytes(plan) bytes (may be
+// null when that is 0); its first kSplitCounterBytes (the arrival counters) must be zero before
+// the first call and are left zero by every completed call.
+constexpr size_t kSplitCounterBytes = 4096;
+struct TcPlan {
+  int bm, stages, tmem_cols, splits, stages_per_split, tiles, a_col0;
+  bool cluster, persist, dbl;
+  size_t partial_bytes;  // fp32 partial tiles of the workspace reduction (0: none)
+};
+TcPlan plan_gemm_tc(int M, int N, int K);
+size_t gemm_tc_workspace_bytes(const TcPlan &plan);
+cudaError_t launch_gemm_tc(const TcPlan &plan, const uint16_t *x, const void *packed, int M, int N, int K, int g,
+                           int dtype, uint16_t *y, int *err, void *workspace, cudaStream_t stream);
 // W4A16_SPLITK_AUTO or W4A16_SPLITK_GLOBAL (include/w4a16.h); returns a W4A16 status.
 int set_splitk_mode(int mode);
+
+// The driver's cuTensorMapEncodeTiled (looked up once); null if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Tied-embedding gather: out[t][k] = W[k][ids[t]] for t < T (grid T x ceil(KT / 8)).
 cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, int N, int g, int dtype,

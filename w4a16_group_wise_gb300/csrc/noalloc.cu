@@ -12,13 +12,20 @@
 //
 // Rules that follow from one shared, static scratch area:
 //  - every call uses the same array, which keeps whatever the last call left in it; the only
-//    part that must start at zero (the arrival counters at its head) is cleared when a device is
-//    first set up, and every call that completes leaves it at zero again;
+//    part that must start at zero (the arrival counters at its head) starts at zero when the
+//    library's device code is loaded, is cleared again (ordered on the caller's stream, before
+//    the call's kernel) when a device is first set up, and is left at zero by every call that
+//    completes;
 //  - calls that overlap on the GPU (on different streams, or from different host threads) race
 //    on the array and give wrong results: serialize them;
 //  - the first call on a device sets it up (looks up the array's device address and clears the
-//    counters, synchronously); make that first call before capturing the stream into a graph;
-//  - problems whose scratch would exceed kScratchBytes are rejected with W4A16_ERR_WORKSPACE.
+//    counters); make that first call before capturing the stream into a graph;
+//  - CUDA loads a library's device code, and with it this array, on a device when the library is
+//    first used there, which may be inside the first call here: that call can then fail for lack
+//    of device memory.  A caller that must not see that make one call at start-up;
+//  - the call plans its launch once and checks that plan's scratch against kScratchBytes, so a
+//    split-K option changed by another thread meanwhile cannot make the kernel use more than was
+//    checked; problems whose scratch would exceed it are rejected with W4A16_ERR_WORKSPACE.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -33,7 +40,7 @@ using namespace w4a16;
 namespace {
 
 constexpr size_t kScratchBytes = (size_t)W4A16_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kCounterBytes = 4096;  // arrival counters at the head of a split-K workspace
+static_assert(kScratchBytes > kSplitCounterBytes, "the scratch holds the split-K arrival counters");
 
 // The scratch itself.  In host code `g_scratch` only names the symbol; its device address comes
 // from cudaGetSymbolAddress, once per device, with that device current.
@@ -43,15 +50,17 @@ constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices];
 std::mutex g_mu;
 
-// Device address of the scratch on the current device (set-up on first use); null on failure.
-void *scratch_on_current_device() {
+// Device address of the scratch on the current device; null on failure.  The first call on a
+// device looks the address up and clears the arrival counters on `stream`, ahead of the kernel
+// the caller launches next on that stream.
+void *scratch_on_current_device(cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return nullptr;
-    if (cudaMemset(p, 0, kCounterBytes) != cudaSuccess) return nullptr;  // counters start at zero
+    if (cudaMemsetAsync(p, 0, kSplitCounterBytes, stream) != cudaSuccess) return nullptr;
     g_scratch_ptr[dev] = p;
   }
   return g_scratch_ptr[dev];
@@ -69,15 +78,21 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t *x, const void *packed, int M, 
   if (M == 0) return W4A16_OK;
   if (!x || !packed || !y) return W4A16_ERR_INVALID;
   if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
-  const size_t need = w4a16_workspace_bytes(M, N, K, g);
+  // one plan per call: the scratch checked here is the scratch the launch uses
+  TcPlan plan = {};
+  size_t need = 0;
+  if (M > kDecodeMaxM) {
+    plan = plan_gemm_tc(M, N, K);
+    need = gemm_tc_workspace_bytes(plan);
+  }
   if (need > kScratchBytes) return W4A16_ERR_WORKSPACE;
-  void *scratch = scratch_on_current_device();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *scratch = scratch_on_current_device(s);
   int *err = device_error_word();
   if (!scratch || !err) return W4A16_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int gl = layout_group(K, g);
   cudaError_t e = (M <= kDecodeMaxM) ? launch_gemv(x, packed, M, N, K, gl, kDtypeF16, y, err, s)
-                                     : launch_gemm_tc(x, packed, M, N, K, gl, kDtypeF16, y, err, scratch, s);
+                                     : launch_gemm_tc(plan, x, packed, M, N, K, gl, kDtypeF16, y, err, scratch, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;
