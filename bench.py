@@ -41,8 +41,8 @@ METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate
 # captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch each of q_k_v, gate_up
 # and down at M=1, summarised under profiles/), keyed by the sha256 of the kernel source they
 # were taken on; reported as null whenever that source has changed since.
-TRAFFIC = {"source_sha256": "5226c4f59f644360a379b12cb7716502a93256257849bddd969bec8d55116b71",
-           "bytes_per_launch": (3299328 + 14200576 + 7120128) // 3}
+TRAFFIC = {"source_sha256": "502c65800c8c9132ffc889669dab283bd26f476d7d30d5e5940dcc60369cb662",
+           "bytes_per_launch": (3299328 + 14200064 + 7119872) // 3}
 
 
 def max_over_ranks(ms, world, device):
@@ -294,6 +294,8 @@ def run_ours(args, rank, world, local_rank):
         prefill = run_prefill(args, w4, torch, dev, stream, layers, timed, bf16, bf16_sus, peak_src)
     with nvtx_range("embed gather and AWQ conversion"):
         embed, convert = run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src)
+    with nvtx_range("repack and dequant"):
+        repack_dequant = run_repack_dequant(args, w4, torch, dev, stream, timed, hbm, peak_src)
     with nvtx_range("bf16 layer"):
         bf16_layer = run_bf16(args, w4, torch, dev, stream, timed, hbm, bf16, bf16_sus, peak_src, rank)
     with nvtx_range("other configurations"):
@@ -312,12 +314,14 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(len(launches), sum(p.numel() for (_, _, _, _, p) in launches) / 1e6, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
-                     "kernel": "gemv_kernel (decode)", "peak_source": peak_src,
-                     "note": "achieved = algorithmic bytes of the step / step time; every launch of the step is the decode kernel"},
+                     "kernel": "decode: gemv_small_kernel (q_k_v, gate_up), gemv_kernel (down)", "peak_source": peak_src,
+                     "note": "achieved = algorithmic bytes of the step / step time (inter-launch gaps included); "
+                             "every launch of the step is one of the two decode kernels"},
         "per_shape": per_shape,
         "prefill": prefill,
         "embed": embed,
         "awq_to_standard": convert,
+        "repack_dequant": repack_dequant,
         "bf16_layer": bf16_layer,
         "configs": configs,
         "e2e": e2e,
@@ -448,6 +452,79 @@ def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
                          "frac": round(gbs / hbm, 4), "peak_source": peak_src}}, convert
 
 
+def run_repack_dequant(args, w4, torch, dev, stream, timed, hbm, peak_src):
+    """Secondary: the one-time repack (AWQ tensors -> packed layout, whole-matrix and in
+    4992-column chunks) and the standalone dequant (packed -> fp16 W [K, N]), in GB/s of bytes
+    read plus bytes written, on the tied LM head (2048 x 131072: inputs larger than L2) and on
+    the gate_up layer (2048 x 13312, cycling through 8 copies so that every call reads from HBM)."""
+    out = {}
+    reps = max(3, min(20, args.steps // 100))
+    for name, copies in (("lm_head", 1), ("gate_up", 8)):
+        K, N = inputs.SHAPES[name]
+        srcs, packs = [], []
+        for i in range(copies):
+            h = inputs.make_weights(K, N, G, seed=700 + i)
+            srcs.append((torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                         torch.from_numpy(h["scales"]).to(dev)))
+            packs.append(torch.empty(w4.packed_bytes(K, N, G), dtype=torch.uint8, device=dev))
+            del h
+        in_bytes = sum(t.numel() * t.element_size() for t in srcs[0])
+        pk_bytes = packs[0].numel()
+        W = torch.empty((K, N), dtype=torch.float16, device=dev)
+        chunk = 4992  # 78 n-blocks; the last chunk of the LM head is ragged (1280 columns)
+
+        def repack_all():
+            with torch.cuda.stream(stream):
+                for (qw, qz, sc), pk in zip(srcs, packs):
+                    w4.repack(qw, qz, sc, K, N, G, packed=pk, stream=stream)
+
+        def repack_chunked():
+            with torch.cuda.stream(stream):
+                for (qw, qz, sc), pk in zip(srcs, packs):
+                    for n0 in range(0, N, chunk):
+                        n1 = min(N, n0 + chunk)
+                        w4.repack_chunk(qw[:, n0 // 8:n1 // 8], qz[:, n0 // 8:n1 // 8], sc[:, n0:n1], K, N, G, n0, n1,
+                                        pk, stream=stream)
+
+        def dequant_all():
+            with torch.cuda.stream(stream):
+                for pk in packs:
+                    w4.dequant(pk, K, N, G, out=W, stream=stream)
+
+        def as_graph(fn):
+            """fn captured once in a CUDA graph: the chunked repack is many short launches, which the
+            host would otherwise not issue fast enough"""
+            fn()
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+
+            def replay():
+                with torch.cuda.stream(stream):
+                    gr.replay()
+            return replay
+
+        res = {"K": K, "N": N, "g": G, "copies": copies, "timing": "CUDA graph of the calls, replayed"}
+        for label, fn, moved in (("repack", repack_all, in_bytes + pk_bytes),
+                                 ("repack_chunked_4992", repack_chunked, in_bytes + pk_bytes),
+                                 ("dequant", dequant_all, pk_bytes + 2 * K * N)):
+            fn = as_graph(fn)
+            fn()
+            stream.synchronize()
+            ms = timed(fn, reps) / (reps * copies)
+            gbs = moved / (ms * 1e-3) / 1e9
+            res[label] = {"us_per_call": round(ms * 1e3, 2), "bytes_moved": moved, "gbs": round(gbs, 1),
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                       "frac": round(gbs / hbm, 4), "peak_source": peak_src}}
+        if w4.last_device_error(stream) != 0:
+            raise RuntimeError("device-side error in the repack / dequant runs")
+        out[name] = res
+        del srcs, packs, W
+    out["metric"] = "GB/s of bytes read + written (repack: AWQ tensors in, packed buffer out; dequant: packed in, fp16 W out)"
+    return out
+
+
 def _x_on_device(torch, dev, M, K, seed, dtype):
     """Seeded activations [M, K] on the device, fp16 or (dtype "bf16") bf16."""
     x = inputs.make_x(M, K, seed=seed, dtype=dtype)
@@ -562,6 +639,33 @@ def _oracle_pass(layer):
         oracle.linear(x.view(np.uint16), h["qweight"], h["qzeros"], h["scales"].view(np.uint16), K, N, G)
 
 
+def host_cpu():
+    """The host CPU: model name, logical cores present and cores this process may run on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        affinity = None
+    return {"model": model or "unknown", "nproc": os.cpu_count(), "sched_getaffinity": affinity}
+
+
 def oracle_sample(budget_s=10.0):
     """Time the CPU oracle, as it stands, on one decoder layer's three linears at M=1."""
     import oracle
@@ -577,7 +681,7 @@ def oracle_sample(budget_s=10.0):
         _oracle_pass(layer)
     dt = (time.perf_counter() - t0) / reps
     return {"value": round(sample_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "host_cpu": host_cpu(),
             "sample": "one decoder layer's q_k_v, gate_up, down at M=1 (%.1f MB algorithmic), %d timed passes "
                       "of %.3f s" % (sample_bytes / 1e6, reps, dt)}
 
@@ -609,13 +713,15 @@ def run_reference(args, rank, world):
               "(%.2f MB algorithmic)" % (cols, step_bytes / 1e6))
     cfg = workload_config()
     cfg["sample"] = sample
+    cfg["note"] = ("the oracle times one decoder layer's three linears (a column slice of each) per step, not the "
+                   "8-layer step: the rate is per algorithmic byte, not the same work")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host_cpu": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -631,26 +737,44 @@ def workload_config(n_launches=3 * LAYERS, packed_mb=None, world=1):
 
 
 def run_profile_case(spec):
-    """A small fixed case for ncu: 2 warm-up launches, then 3 launches (capture with -s 2 -c 3)."""
+    """A small fixed case for ncu: [OP:]SHAPE:M with OP gemm (default; M rows of x), repack,
+    dequant or embed (M token ids); 2 warm-up launches, then 3 launches (capture with -s 2 -c 3)."""
     import torch
     import __graft_entry__
     import w4a16_group_wise_gb300 as w4
 
     __graft_entry__.build()
-    name, M = spec.split(":")
-    M = int(M)
+    parts = spec.split(":")
+    op = parts[0] if len(parts) == 3 else "gemm"
+    name, M = parts[-2], int(parts[-1])
     K, N = inputs.SHAPES[name]
     dev = torch.device("cuda", 0)
     h = inputs.make_weights(K, N, G, seed=0)
-    packed = w4.repack(torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
-                       torch.from_numpy(h["scales"]).to(dev), K, N, G)
-    x = torch.from_numpy(inputs.make_x(M, K, seed=0)).to(dev)
-    y = torch.empty((M, N), dtype=torch.float16, device=dev)
-    for _ in range(5):
-        w4.gemm(x, packed, M, N, K, G, y=y)
+    qw, qz, sc = (torch.from_numpy(h["qweight"]).to(dev), torch.from_numpy(h["qzeros"]).to(dev),
+                  torch.from_numpy(h["scales"]).to(dev))
+    packed = w4.repack(qw, qz, sc, K, N, G)
+    if op == "gemm":
+        x = torch.from_numpy(inputs.make_x(M, K, seed=0)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for _ in range(5):
+            w4.gemm(x, packed, M, N, K, G, y=y)
+    elif op == "repack":
+        for _ in range(5):
+            w4.repack(qw, qz, sc, K, N, G, packed=packed)
+    elif op == "dequant":
+        W = torch.empty((K, N), dtype=torch.float16, device=dev)
+        for _ in range(5):
+            w4.dequant(packed, K, N, G, out=W)
+    elif op == "embed":
+        ids = torch.from_numpy(np.random.default_rng(0).integers(0, N, M).astype(np.int32)).to(dev)
+        out = torch.empty((M, K), dtype=torch.float16, device=dev)
+        for _ in range(5):
+            w4.embed(ids, packed, K, N, G, out=out)
+    else:
+        raise ValueError("unknown profile op %r" % op)
     torch.cuda.synchronize()
     assert w4.last_device_error() == 0
-    print("profile case %s M=%d done" % (name, M))
+    print("profile case %s %s M=%d done" % (op, name, M))
 
 
 def main():
@@ -660,9 +784,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", metavar="SHAPE:M", default=None,
+    ap.add_argument("--profile", metavar="[OP:]SHAPE:M", default=None,
                     help="no timing: repack one layer of SHAPE (qkv, gate_up, down, lm_head, ...) and run "
-                         "a few gemm launches with M rows, for a profiler to capture")
+                         "a few launches of OP (gemm with M rows, the default; repack; dequant; embed of M "
+                         "ids), for a profiler to capture")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
 

@@ -432,7 +432,7 @@ def test_gemm_workspace_too_small_is_rejected(splitk_global):
     assert e.value.status == w4.binding.ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 512), ("qkv", 129), ("square", 40), ("down", 64),
+@pytest.mark.parametrize("name,M", [("down", 512), ("qkv", 256), ("qkv", 129), ("square", 40), ("down", 64),
                                     ("down", 40)])
 def test_gemm_split_k_cluster_matches_workspace_reduction(name, M):
     """The cluster reduction (distributed shared memory, no workspace) and the workspace

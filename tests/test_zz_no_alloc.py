@@ -24,11 +24,11 @@ def _call(x, packed, M, N, K, g, y):
     return binding.lib().w4a16_gemm_noalloc(P(x.data_ptr()), P(packed.data_ptr()), M, N, K, g, P(y.data_ptr()), st)
 
 
-# split-K shapes (scratch in use), a shape that needs none, the decode path, the N = 80 tail
-CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 512, 128), ("square", 40, 128),
+# split-K shapes (scratch in use), shapes that need none, the decode path, the N = 80 tail
+CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 256, 128), ("qkv", 512, 128), ("square", 40, 128),
          ("gate_up", 512, 128), ("gate_up", 1, 128), ("tail80", 17, 32)]
 # the cases that split K: under the workspace reduction they run through the built-in scratch
-SPLIT = {("down", 512), ("qkv", 129), ("qkv", 512), ("square", 40)}
+SPLIT = {("down", 512), ("qkv", 129), ("qkv", 256), ("square", 40)}
 
 _refs = {}
 

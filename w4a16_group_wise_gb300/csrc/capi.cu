@@ -4,6 +4,7 @@
 // "Add cpu_int4 ...": two paths over one set of weights), and the per-device error word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -18,21 +19,26 @@ static __device__ int g_device_error;
 
 namespace {
 constexpr int kMaxDevices = 64;
-int *g_err_ptr[kMaxDevices];
+std::atomic<int *> g_err_ptr[kMaxDevices];
 std::mutex g_err_mu;
 }  // namespace
 
-// The per-device error word of the current device (resolved once per device).
+// The per-device error word of the current device (resolved once per device; later calls read
+// the cached address without taking the lock).
 int *w4a16::device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int *p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
   std::lock_guard<std::mutex> lock(g_err_mu);
-  if (!g_err_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int *>(p);
+  p = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    void *q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_device_error) != cudaSuccess) return nullptr;
+    p = static_cast<int *>(q);
+    g_err_ptr[dev].store(p, std::memory_order_release);
   }
-  return g_err_ptr[dev];
+  return p;
 }
 
 // The group size the packed layout uses for a caller's g: g itself for 32, 64, 128 (K % g == 0);

@@ -791,16 +791,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 namespace {
 
 int sm_count_tc() {
-  static int count[64];
+  static std::atomic<int> count[64];  // per device, 0 until looked up
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
-  if (!count[dev]) {
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (!n) {
     int c = 0;
     cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    count[dev] = c > 0 ? c : 148;
+    n = c > 0 ? c : 148;
+    count[dev].store(n, std::memory_order_relaxed);
   }
-  return count[dev];
+  return n;
 }
 
 // Workspace of a split-K launch with the workspace reduction: kCounterBytes of per-tile
@@ -864,6 +866,17 @@ TcPlan plan_gemm_tc(int M, int N, int K) {
   p.dbl = false;
   p.tmem_cols = kTmemCols;
   int tiles = ntn * ((M + p.bm - 1) / p.bm);
+  // Too few 256-row tiles to cover the GPU, but enough 128-row tiles to cover half of it: take the
+  // half-height tiles and no K split.  Measured at M = 512: q_k_v (48 tiles at BM = 256, two K
+  // splits) went from 14.4 to 13.2 us with 96 whole-K tiles; down (32 tiles, four splits) went
+  // from 19.5 to 21.5 us with 64 half-height tiles and two splits, so there BM stays 256.
+  if (p.bm == 256 && 4 * tiles < 3 * sms) {
+    const int tiles128 = ntn * ((M + 127) / 128);
+    if (2 * tiles128 >= sms) {
+      p.bm = 128;
+      tiles = tiles128;
+    }
+  }
   // Split K when the tiles alone would leave a quarter of the SMs or more idle; keep at least
   // two 128-k stages per split and at most one cluster's worth of splits.  Where the device runs
   // clusters, all clusters of the launch must be resident at once (measured: a second wave of
@@ -908,23 +921,52 @@ int set_splitk_mode(int mode) {
 
 namespace {
 
+// The TMA map of x (K-major, 128-byte swizzle, boxes of 64 k x bm rows; zero fill past M and K).
+// Encoding one costs a driver call, so each host thread keeps the last few it made, keyed by
+// everything the map depends on; a call with the same x buffer and shape reuses it.
+template <class T>
+bool x_tensor_map(CUtensorMap &map, const uint16_t *x, int M, int K, int bm) {
+  struct Entry {
+    const void *x;
+    int M, K, bm, dtype;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int key_dtype = T::kDtype * 256 + dev;  // the element type and the device
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry &e = cache[i];
+    if (e.x == x && e.M == M && e.K == K && e.bm == bm && e.dtype == key_dtype) {
+      map = e.map;
+      return true;
+    }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)bm};
+  const cuuint32_t es[2] = {1, 1};
+  const CUtensorMapDataType xtype = T::kDtype == kDtypeBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (enc(&map, xtype, 2, const_cast<uint16_t *>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry &e = cache[next];
+  next = (next + 1) % kEntries;
+  e = Entry{x, M, K, bm, key_dtype, map};
+  return true;
+}
+
 template <class T>
 cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *packed, int M, int N, int K, int g,
                              uint16_t *y, int *err, void *workspace, cudaStream_t stream) {
   const GemmSmem L = gemm_smem(P.bm, P.stages);
 
-  auto enc = tensor_map_encoder();
-  if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)P.bm};
-  const cuuint32_t es[2] = {1, 1};
-  const CUtensorMapDataType xtype = T::kDtype == kDtypeBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (enc(&map, xtype, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  if (!x_tensor_map<T>(map, x, M, K, P.bm)) return cudaErrorInvalidValue;
 
   SplitPlan sp;
   sp.splits = P.splits;
@@ -939,13 +981,13 @@ cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *pac
   sp.counters = global ? static_cast<int *>(workspace) : nullptr;
   sp.partials = global ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
 
-  static bool configured[64];
+  static std::atomic<bool> configured[64];  // per device: the attribute has been set
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = P.persist ? dim3(std::min(P.tiles, sm_count_tc())) : dim3(sp.ntn, sp.ntm, P.splits);

@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "dq.cuh"
 #include "kernels.h"
@@ -503,30 +504,32 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
 }
 
 int sm_count() {
-  static int count[64];
+  static std::atomic<int> count[64];  // per device, 0 until looked up
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
-  if (!count[dev]) {
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (!n) {
     int c = 0;
     cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    count[dev] = c > 0 ? c : 148;
+    n = c > 0 ? c : 148;
+    count[dev].store(n, std::memory_order_relaxed);
   }
-  return count[dev];
+  return n;
 }
 
 template <class T, int RT, int MB, bool FACTOR>
 cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, const uint8_t *packed, int M, int N,
                            int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
   const int smem = W * RT * MB * 4 * 32 * 4;
-  static bool configured[64];
+  static std::atomic<bool> configured[64];  // per device: the attribute has been set
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, RT, MB, FACTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          160 * 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((tiles + RT - 1) / RT, mblocks);

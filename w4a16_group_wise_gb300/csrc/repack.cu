@@ -47,60 +47,61 @@ __global__ void __launch_bounds__(256) repack_kernel(
     reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
   }
 
-  // Stage the 128 x 8 AWQ words of this chunk (rows past K and columns past N read as 0).
-  __shared__ uint32_t in[kTileK][8];
+  // The chunk's 128 x 8 AWQ words (rows past K and columns past N read as 0), a row's 8 words by 8
+  // consecutive threads (32 contiguous bytes); the row stride of 9 words keeps the reads of the
+  // transposition below free of bank conflicts.  Also the zero words of the chunk's groups.
+  const int gpc = kTileK / g;  // groups per chunk
+  const int G = K / g;
+  __shared__ uint32_t in[kTileK][9];
+  __shared__ uint32_t out[kBlockN][17];  // the chunk's code words (row stride 17: no bank conflicts)
+  __shared__ uint32_t zin[4][8];                         // [group of the chunk][AWQ zero word]
   for (int i = threadIdx.x; i < kTileK * 8; i += blockDim.x) {
-    int kk = i >> 3, c = i & 7;
-    int k = kb + kk, n = b * kBlockN + 8 * c;
-    uint32_t w = 0;
-    if (k < K && n < N) w = (uint32_t)qweight[(int64_t)k * ldq + (n - n0) / 8];
-    in[kk][c] = w;
+    const int kk = i >> 3, c = i & 7;
+    const int k = kb + kk, n = b * kBlockN + 8 * c;
+    in[kk][c] = (k < K && n < N) ? (uint32_t)__ldg(qweight + (int64_t)k * ldq + (n - n0) / 8) : 0u;
+  }
+  if (threadIdx.x < gpc * 8) {
+    const int l = threadIdx.x >> 3, c = threadIdx.x & 7;
+    const int grp = t * gpc + l, n = b * kBlockN + 8 * c;
+    const int sg = (grp * g) / gsrc;
+    zin[l][c] = (grp < G && n < N) ? (uint32_t)__ldg(qzeros + (int64_t)sg * ldz + (n - n0) / 8) : 0u;
   }
   __syncthreads();
 
-  // Codes: row r (column 64b + r), word w covers k = kb + 8w + slot_k(j) in slot j.
-  uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
+  // Codes: row r (column 64b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  Threads take r
+  // fastest, so a warp reads 4 distinct words per step (the rest are broadcasts).
   for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x) {
-    int r = i >> 4, w = i & 15;
-    int c = r >> 3, in_slot = awq_slot_of_col(r & 7);
-    uint32_t out = 0;
+    const int r = i & (kBlockN - 1), w = i >> 6;
+    const int c = r >> 3, sh = 4 * awq_slot_of_col(r & 7);
+    uint32_t o = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t code = (in[8 * w + slot_k(j)][c] >> (4 * in_slot)) & 0xFu;
-      out |= code << (4 * j);
-    }
-    codes[i] = out;
+    for (int j = 0; j < 8; ++j) o |= ((in[8 * w + slot_k(j)][c] >> sh) & 0xFu) << (4 * j);
+    out[r][w] = o;
   }
+  __syncthreads();
+  // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
+  uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
+  for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x) codes[i] = out[i >> 4][i & 15];
 
   // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
   // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
   // source tensors (gsrc == g, or gsrc == K for one group over all of K).
-  const int gpc = kTileK / g;  // groups per chunk
-  const int G = K / g;
   for (int i = threadIdx.x; i < gpc * kBlockN; i += blockDim.x) {
-    int l = i / kBlockN, p = i % kBlockN;
-    int grp = t * gpc + l, n = b * kBlockN + meta_row(p);
-    int sg = (grp * g) / gsrc;
-    uint16_t s = 0;
-    if (grp < G && n < N) s = scales[(int64_t)sg * lds + (n - n0)];
-    reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes)[p] = s;
+    const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r, read in order
+    const int grp = t * gpc + l, n = b * kBlockN + r;
+    const int sg = (grp * g) / gsrc;
+    const uint16_t sv = (grp < G && n < N) ? scales[(int64_t)sg * lds + (n - n0)] : (uint16_t)0;
+    reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes)[meta_pos(r)] = sv;
   }
-  for (int i = threadIdx.x; i < gpc * 8; i += blockDim.x) {
-    int l = i / 8, wi = i % 8;
-    int grp = t * gpc + l;
-    int sg = (grp * g) / gsrc;
-    uint32_t out = 0;
+  if (threadIdx.x < gpc * 8) {
+    const int l = threadIdx.x >> 3, wi = threadIdx.x & 7;
+    uint32_t o = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      int n = b * kBlockN + meta_row(8 * wi + j);
-      uint32_t z = 0;
-      if (grp < G && n < N) {
-        uint32_t zw = (uint32_t)qzeros[(int64_t)sg * ldz + (n - n0) / 8];
-        z = (zw >> (4 * awq_slot_of_col(n & 7))) & 0xFu;
-      }
-      out |= z << (4 * j);
+      const int r = meta_row(8 * wi + j);
+      o |= ((zin[l][r >> 3] >> (4 * awq_slot_of_col(r & 7))) & 0xFu) << (4 * j);
     }
-    reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes)[wi] = out;
+    reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes)[wi] = o;
   }
 }
 
