@@ -10,9 +10,12 @@ Metric: effective HBM GB/s at M=1 = algorithmic bytes / time, algorithmic bytes 
 K*N/2 (codes) + (K/g)*N*(0.5 + 2) (zeros, scales) + 2*M*K (x) + 2*M*N (y).  A secondary block
 reports the M=512 prefill shapes in TFLOP/s (2*M*N*K per linear).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-Under torchrun (N > 1) every rank runs its own replica on its own GPU (the layer does not
-shard across GPUs here: "replicas only"); value = all ranks' bytes / the slowest rank's time.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--shard]
+Under torchrun (N > 1) every rank runs its own replica on its own GPU by default (weak scaling);
+value = all ranks' bytes / the slowest rank's time.  With --shard the ranks split every linear's
+output columns instead (column-parallel, strong scaling: the step's total bytes are fixed); the
+ranks exchange nothing on the data path, and value = the step's total bytes / the slowest rank's
+time.
 """
 import argparse
 import ctypes
@@ -166,17 +169,25 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     hbm, bf16, bf16_sus, peak_src = peaks()
 
-    # ---------------- resident weights: LAYERS copies of the three decoder linears
+    # ---------------- resident weights: LAYERS copies of the three decoder linears (with --shard,
+    # the same layers on every rank, each rank holding its own columns of each)
+    sharded = args.shard
     layers = []
     with torch.cuda.stream(stream):
         for li in range(LAYERS):
             lin = []
             for name, K, N in DECODE_SHAPES:
-                h = inputs.make_weights(K, N, G, seed=1000 * rank + 10 * li + len(lin))
+                seed = (0 if sharded else 1000 * rank) + 10 * li + len(lin)
+                h = inputs.make_weights(K, N, G, seed=seed)
                 qw = torch.from_numpy(h["qweight"]).to(dev)
                 qz = torch.from_numpy(h["qzeros"]).to(dev)
                 sc = torch.from_numpy(h["scales"]).to(dev)
-                packed = w4.repack(qw, qz, sc, K, N, G, stream=stream)
+                if sharded:
+                    n0, n1 = w4.column_slices(N, world)[rank]
+                    packed = w4.repack_slice(qw, qz, sc, K, N, G, n0, n1, stream=stream)
+                    N = n1 - n0
+                else:
+                    packed = w4.repack(qw, qz, sc, K, N, G, stream=stream)
                 lin.append((name, K, N, packed))
                 del qw, qz, sc
             layers.append(lin)
@@ -226,7 +237,17 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk, nvtx_range("decode step (timed)"):
         ms = timed(replay, args.steps)
     ms_step = ms / args.steps
-    value = whole_job_rate(step_bytes, world, ms_step) / 1e9
+    if sharded:
+        job_bytes = torch.tensor([float(step_bytes)], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(job_bytes)
+        job_bytes = float(job_bytes.item())
+        value = job_bytes / (ms_step * 1e-3) / 1e9
+    else:
+        value = whole_job_rate(step_bytes, world, ms_step) / 1e9
+    if sharded:
+        return run_sharded_tail(args, w4, torch, dev, stream, launches, xs, ys, timed, clk, ms_step, value,
+                                job_bytes, step_bytes, hbm, peak_src, world)
 
     # ---------------- per-shape kernel times (8 launches of one shape per graph replay)
     per_shape = {}
@@ -329,6 +350,58 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     return result
+
+
+def run_sharded_tail(args, w4, torch, dev, stream, launches, xs, ys, timed, clk, ms_step, value, job_bytes,
+                     rank_bytes, hbm, peak_src, world):
+    """The column-parallel step's line: the job's rate, this rank's roofline, and e2e (each rank
+    copies x in and its columns of y out around its C-ABI calls; no gather of y)."""
+    M = 1
+    x_host = torch.cat([x.view(-1) for x in xs]).cpu().pin_memory()
+    y_host = torch.empty(sum(y.numel() for y in ys), dtype=torch.float16).pin_memory()
+    x_dev = torch.empty_like(x_host, device=dev)
+    y_dev = torch.empty_like(y_host, device=dev)
+    gemm_c = w4.binding.lib().w4a16_gemm
+    vp = ctypes.c_void_p
+    st = vp(stream.cuda_stream)
+    e2e_args, ox, oy = [], 0, 0
+    for (_, _, K, N, packed) in launches:
+        e2e_args.append((vp(x_dev[ox:].data_ptr()), vp(packed.data_ptr()), M, N, K, G, vp(y_dev[oy:].data_ptr()),
+                         vp(0), 0, st))
+        ox += M * K
+        oy += M * N
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            for a in e2e_args:
+                rc = gemm_c(*a)
+                if rc != 0:
+                    raise w4.W4A16Error("w4a16_gemm", rc)
+            y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps) / args.steps
+    achieved = rank_bytes / (ms_step * 1e-3) / 1e9
+    cfg = workload_config(len(launches), None, world)
+    cfg["parallelism"] = "column-parallel over %d GPUs (each linear's N split on 64-column boundaries; no " \
+                         "collective on the data path)" % world
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; AWQ codes uniform 0..15, scales U[0.002,0.02] fp16, x N(0,1) fp16)",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_src,
+                     "kernel": "decode: gemv_small_kernel / gemv_kernel on rank 0's column slices"},
+        "e2e": {"value": round(job_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clk.summary(),
+    }
 
 
 def run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src):
@@ -784,6 +857,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shard", action="store_true",
+                    help="with N > 1: split every linear's output columns across the ranks (strong "
+                         "scaling) instead of running a replica per rank")
     ap.add_argument("--profile", metavar="[OP:]SHAPE:M", default=None,
                     help="no timing: repack one layer of SHAPE (qkv, gate_up, down, lm_head, ...) and run "
                          "a few launches of OP (gemm with M rows, the default; repack; dequant; embed of M "

@@ -1,8 +1,9 @@
-"""The N > 1 path of bench.py on CPU: two gloo ranks on 127.0.0.1.
+"""The N > 1 paths on CPU: two gloo ranks on 127.0.0.1.
 
-Every GPU runs its own replica of the benchmark step (the layer does not shard across GPUs
-here), so the only cross-rank logic is the timing: the job's time is the slowest rank's, and the
-job's rate counts every rank's units.  The reference arm runs on rank 0 only.
+- bench.py's timing: the job's time is the slowest rank's, and the job's rate counts every
+  rank's units; the reference arm runs on rank 0 only.
+- The column-parallel split (w4a16_group_wise_gb300.shard): the ranks' column ranges partition
+  [0, N) on 64-column boundaries, and gathering every rank's columns of y rebuilds y whole.
 """
 import argparse
 import os
@@ -63,3 +64,66 @@ def test_one_rank_is_unchanged():
     import bench
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
     assert bench.whole_job_rate(7.0, 1, 2.0) == pytest.approx(3500.0)
+
+
+def _shard_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from w4a16_group_wise_gb300 import shard
+    out = {}
+    for N in (13312, 3072, 80, 131072, 2048 + 8):
+        mine = shard.column_slices(N, world)[rank]
+        every = [None] * world
+        dist.all_gather_object(every, mine)
+        out[N] = every
+    # gather of y: every rank fills its columns of a known y; the gathered y is y whole
+    M, N = 3, 200
+    part = shard.ColumnParallelLinear.__new__(shard.ColumnParallelLinear)
+    part.slices, part.world = shard.column_slices(N, world), world
+    n0, n1 = part.slices[rank]
+    y_full = torch.arange(M * N, dtype=torch.float32).reshape(M, N)
+    y_gathered = part.gather(y_full[:, n0:n1].contiguous())
+    dist.barrier()
+    q.put((rank, out, bool(torch.equal(y_gathered, y_full))))
+    dist.destroy_process_group()
+
+
+def test_two_ranks_split_the_columns_and_gather_y():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0][1] == res[1][1]                   # both ranks see the same partition
+    for N, slices in res[0][1].items():
+        assert slices[0][0] == 0 and slices[-1][1] == N
+        for (a0, a1), (b0, b1) in zip(slices, slices[1:]):
+            assert a1 == b0                          # contiguous, disjoint
+        for n0, n1 in slices:
+            assert n0 % 64 == 0 and n0 <= n1        # n-block aligned starts
+            assert n1 == N or n1 % 64 == 0          # only the last end is ragged
+        widths = [n1 - n0 for n0, n1 in slices]
+        assert max(widths) - min(widths) <= 64      # balanced to one n-block
+    assert res[0][1][80] == [(0, 64), (64, 80)]     # the 64 + 16 layer: the tail on the last rank
+    assert all(ok for _, _, ok in res)
+
+
+def test_column_slices_edge_cases():
+    import sys
+    sys.path.insert(0, ROOT)
+    from w4a16_group_wise_gb300 import shard
+    assert shard.column_slices(80, 4) == [(0, 0), (0, 0), (0, 64), (64, 80)]   # more ranks than n-blocks
+    assert shard.column_slices(64, 1) == [(0, 64)]
+    assert shard.column_slices(13312, 8) == [(1664 * r, 1664 * (r + 1)) for r in range(8)]
+    assert shard.column_slices(2056, 2) == [(0, 1024), (1024, 2056)]
+    with pytest.raises(ValueError):
+        shard.column_slices(0, 2)

@@ -8,3 +8,4 @@ tensors into it.  ``inputs`` draws the seeded synthetic tensors used by tests an
 from .binding import (W4A16Error, awq_to_standard, dequant, embed, gemm, gemm_noalloc, last_device_error, layout_version,  # noqa: F401
                       packed_bytes, repack, repack_chunk, selftest_wait_timeout, set_option, status_string,
                       workspace_bytes)
+from .shard import ColumnParallelLinear, column_slices, repack_slice  # noqa: F401
