@@ -232,6 +232,26 @@ int w4a16_embed_bf16(const int32_t *ids, int T, const void *packed, int K, int N
  * dequantize prefill weights from the tinygemm layout, not a copy"). */
 int w4a16_selftest_wait_timeout(int64_t limit_ns, int *status, void *stream);
 
+/* 1 if this library is the bounds-checked debug build, else 0.  That build (the same sources
+ * compiled with W4A16_BOUNDS defined, shipped as _libw4a16_bounds.so beside the normal library,
+ * with the same entry points) checks every global read of the packed weights, x, ids and the AWQ
+ * tensors, and every global write of y, W, out and the split-K workspace, against the extent of
+ * its buffer as the call's arguments define it (w4a16_packed_bytes for a packed buffer, M*K
+ * elements for x, M*N for y, the slices' rows times their strides for w4a16_repack_chunk, ...).
+ * An access outside it is skipped (a read gives zeros) and recorded in the device error word:
+ * w4a16_last_device_error then returns W4A16_ERR_DEVICE.  Nothing traps.  It stands in for a
+ * memory checker (the test strategy's "Race detection / sanitizers"); it is slower and is not
+ * meant for production. */
+int w4a16_bounds_checked(void);
+
+/* Self-test of the bounds check, dereferencing nothing: one thread runs the check on five fixed
+ * (offset, size, extent) cases, two inside their buffer and three outside (one byte past the end,
+ * one byte before the start, any byte of an empty buffer), and writes to *status (a 4-byte aligned
+ * device int) bit i for each case judged outside.  The bounds-checked build writes 0x1C and
+ * records the misses in the device error word; the normal build, whose check is compiled out,
+ * writes 0 and records nothing. */
+int w4a16_selftest_bounds(int *status, void *stream);
+
 /* Static description of a status code. */
 const char *w4a16_status_string(int status);
 

@@ -34,10 +34,19 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) <= set(binding.SIGNATURES)
 
 
-def test_exports_nothing_undeclared():
-    out = os.popen("nm -D --defined-only %s" % binding.LIB_PATH).read()
+@pytest.mark.parametrize("path", [binding.LIB_PATH, binding.BOUNDS_LIB_PATH])
+def test_exports_nothing_undeclared(L, path):
+    """The normal library and its bounds-checked build export the same declared entry points."""
+    out = os.popen("nm -D --defined-only %s" % path).read()
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l and "w4a16" in l}
     assert exported == set(_declared())
+
+
+def test_which_build(L):
+    assert L.w4a16_bounds_checked() == 0
+    with binding.bounds_checked_library() as B:
+        assert B.w4a16_bounds_checked() == 1 and binding.lib() is B
+    assert binding.lib() is L
 
 
 def test_layout_version_and_sizes(L):

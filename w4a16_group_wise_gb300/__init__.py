@@ -5,7 +5,7 @@
 The compute is a C-ABI CUDA library (include/w4a16.h, csrc/); ``binding`` marshals torch
 tensors into it.  ``inputs`` draws the seeded synthetic tensors used by tests and benchmarks.
 """
-from .binding import (W4A16Error, awq_to_standard, dequant, embed, gemm, gemm_noalloc, last_device_error, layout_version,  # noqa: F401
-                      packed_bytes, repack, repack_chunk, selftest_wait_timeout, set_option, status_string,
-                      workspace_bytes)
+from .binding import (W4A16Error, awq_to_standard, bounds_checked, bounds_checked_library, dequant, embed,  # noqa: F401
+                      gemm, gemm_noalloc, last_device_error, layout_version, packed_bytes, repack, repack_chunk,
+                      selftest_bounds, selftest_wait_timeout, set_option, status_string, workspace_bytes)
 from .shard import ColumnParallelLinear, column_slices, repack_slice  # noqa: F401

@@ -5,6 +5,7 @@ tensors into device pointers and the current CUDA stream into a stream handle, a
 outputs when the caller does not pass them, and raises on a non-zero status.  There is no CPU
 fallback: if the shared library is missing or fails to load, every call raises.
 """
+import contextlib
 import ctypes
 import os
 
@@ -12,6 +13,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_libw4a16.so")
+BOUNDS_LIB_PATH = os.path.join(_HERE, "_libw4a16_bounds.so")  # the bounds-checked debug build
 
 OK = 0
 ERR_INVALID = -1
@@ -47,12 +49,15 @@ SIGNATURES = {
     "w4a16_gemm_bf16": ([_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "w4a16_dequant_bf16": ([_P, _I, _I, _I, _P, _P], _I),
     "w4a16_embed_bf16": ([_P, _I, _P, _I, _I, _I, _P, _P], _I),
+    "w4a16_bounds_checked": ([], _I),
+    "w4a16_selftest_bounds": ([_P, _P], _I),
 }
 
 # element type of a layer -> suffix of its entry points
 _SUFFIX = {torch.float16: "", torch.bfloat16: "_bf16"}
 
-_lib = None
+_libs = {}              # path -> loaded library
+_active = [LIB_PATH]    # the library calls go to: the last entry
 
 
 class W4A16Error(RuntimeError):
@@ -61,19 +66,37 @@ class W4A16Error(RuntimeError):
         super().__init__("%s failed: %d (%s)" % (fn, status, status_string(status)))
 
 
-def lib():
-    """The loaded CUDA library; raises if it has not been built."""
-    global _lib
-    if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("CUDA library %s is missing: run __graft_entry__.build() first" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
+def _load(path):
+    L = _libs.get(path)
+    if L is None:
+        if not os.path.exists(path):
+            raise RuntimeError("CUDA library %s is missing: run __graft_entry__.build() first" % path)
+        L = ctypes.CDLL(path)
         for name, (args, res) in SIGNATURES.items():
             f = getattr(L, name)
             f.argtypes = args
             f.restype = res
-        _lib = L
-    return _lib
+        _libs[path] = L
+    return L
+
+
+def lib():
+    """The loaded CUDA library (the normal build, or the bounds-checked one inside
+    bounds_checked_library()); raises if it has not been built."""
+    return _load(_active[-1])
+
+
+@contextlib.contextmanager
+def bounds_checked_library():
+    """Within the block, every call of this module goes to the bounds-checked debug build, whose
+    kernels check each global access against its buffer's extent (a miss is skipped and makes
+    last_device_error() raise).  Its device error word and first-use state are its own."""
+    L = _load(BOUNDS_LIB_PATH)
+    _active.append(BOUNDS_LIB_PATH)
+    try:
+        yield L
+    finally:
+        _active.pop()
 
 
 def status_string(status):
@@ -238,6 +261,19 @@ def selftest_wait_timeout(limit_ns=1_000_000, stream=None):
     _check("w4a16_selftest_wait_timeout", lib().w4a16_selftest_wait_timeout(int(limit_ns), _ptr(status),
                                                                            _stream(stream)))
     return int(status.item())
+
+
+def selftest_bounds(stream=None):
+    """The bounds check on five fixed cases (see include/w4a16.h): returns the bitmask of cases
+    judged outside their buffer (0x1C in the bounds-checked build, 0 in the normal one)."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check("w4a16_selftest_bounds", lib().w4a16_selftest_bounds(_ptr(status), _stream(stream)))
+    return int(status.item())
+
+
+def bounds_checked():
+    """True when calls go to the bounds-checked debug build."""
+    return bool(lib().w4a16_bounds_checked())
 
 
 def last_device_error(stream=None):

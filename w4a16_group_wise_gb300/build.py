@@ -1,8 +1,9 @@
-"""Build the CUDA library (sm_103a) in-tree: csrc/*.cu -> _libw4a16.so beside this file.
+"""Build the CUDA library (sm_103a) in-tree: csrc/*.cu -> _libw4a16.so beside this file, and its
+bounds-checked debug build (the same sources with W4A16_BOUNDS defined) -> _libw4a16_bounds.so.
 
-Plain nvcc, no cmake: every translation unit is compiled in parallel with one -gencode, then
-linked into a shared library with the CUDA runtime linked statically.  The result exports
-exactly the extern "C" entry points of include/w4a16.h.
+Plain nvcc, no cmake: every translation unit of both libraries is compiled in parallel with one
+-gencode, then each set is linked into a shared library with the CUDA runtime linked statically.
+Each library exports exactly the extern "C" entry points of include/w4a16.h.
 """
 import concurrent.futures as cf
 import os
@@ -15,6 +16,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "_libw4a16.so")
+BOUNDS_LIB = os.path.join(HERE, "_libw4a16_bounds.so")
+# library -> (object directory, extra defines)
+VARIANTS = {LIB: (OUT_DIR, []), BOUNDS_LIB: (os.path.join(OUT_DIR, "bounds"), ["-DW4A16_BOUNDS"])}
 SOURCES = ["capi.cu", "repack.cu", "dequant.cu", "gemv.cu", "gemm_tc.cu", "noalloc.cu", "embed.cu", "convert.cu",
            "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,42 +39,49 @@ def _inputs():
     return files
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs() + [os.path.abspath(__file__)])
 
 
 def build(force=False, verbose=False, ptxas_info=False):
-    """Compile and link if any input is newer than the library.  Returns the library path."""
-    if not force and not _stale():
+    """Compile and link each library that is missing or older than an input.  Returns the path
+    of the normal library."""
+    todo = [lib for lib in VARIANTS if force or _stale(lib)]
+    if not todo:
         return LIB
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc] + ARCH + FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        lib, src = job
+        out_dir, defines = VARIANTS[lib]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc] + ARCH + FLAGS + defines + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         if r.returncode != 0:
-            raise RuntimeError("nvcc failed on %s:\n%s" % (src, r.stdout))
+            raise RuntimeError("nvcc failed on %s%s:\n%s" % (src, " ".join([""] + defines), r.stdout))
         return obj, r.stdout
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    for lib in todo:
+        os.makedirs(VARIANTS[lib][0], exist_ok=True)
+    jobs = [(lib, src) for lib in todo for src in SOURCES]
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), max(os.cpu_count() or 1, 4))) as ex:
+        results = list(ex.map(compile_one, jobs))
     if verbose or ptxas_info:
         for (_, log) in results:
             if log.strip():
                 print(log)
-    objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
-    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("link failed:\n%s" % r.stdout)
-    os.replace(tmp, LIB)
+    for lib in todo:
+        objs = [o for (l, _), (o, _) in zip(jobs, results) if l == lib]
+        tmp = lib + ".tmp"
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
+        r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed:\n%s" % r.stdout)
+        os.replace(tmp, lib)
     return LIB
 
 

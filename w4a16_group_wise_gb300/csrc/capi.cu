@@ -85,8 +85,10 @@ int repack_chunk_impl(const int32_t *qweight_c, int64_t ld_qweight, const int32_
     return W4A16_ERR_MISALIGNED;
   const int gl = layout_group(K, g);
   const int gsrc = (g == -1) ? K : g;  // rows of K per row of the source scales and zeros
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
   return map_launch(launch_repack(qweight_c, ld_qweight, qzeros_c, ld_qzeros, scales_c, ld_scales, K, N, gl, gsrc,
-                                  dtype, n0, n1, packed, static_cast<cudaStream_t>(stream)));
+                                  dtype, n0, n1, packed, err, static_cast<cudaStream_t>(stream)));
 }
 
 int repack_impl(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales, int K, int N, int g,
@@ -156,7 +158,7 @@ extern "C" {
 
 size_t w4a16_packed_bytes(int K, int N, int g) {
   if (check_shape(K, N, g) != W4A16_OK) return 0;
-  return (size_t)kHeaderBytes + (size_t)num_nblocks(N) * num_ktiles(K) * chunk_bytes(layout_group(K, g));
+  return (size_t)packed_extent(K, N, layout_group(K, g));
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K, int g) {
@@ -218,7 +220,9 @@ int w4a16_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq,
       !aligned16(qweight_std) || (reinterpret_cast<uintptr_t>(qzeros_std) & 3u))
     return W4A16_ERR_MISALIGNED;
   const int zero_rows = (g == -1 || g == K) ? 1 : K / g;
-  return map_launch(launch_awq_to_standard(qweight_awq, qzeros_awq, K, N, zero_rows, qweight_std, qzeros_std,
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_awq_to_standard(qweight_awq, qzeros_awq, K, N, zero_rows, qweight_std, qzeros_std, err,
                                            static_cast<cudaStream_t>(stream)));
 }
 
@@ -273,6 +277,16 @@ int w4a16_selftest_wait_timeout(int64_t limit_ns, int *status, void *stream) {
   int *err = device_error_word();
   if (!err) return W4A16_ERR_CUDA;
   return map_launch(launch_wait_timeout((uint64_t)limit_ns, status, err, static_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_bounds_checked(void) { return bounds_checked() ? 1 : 0; }
+
+int w4a16_selftest_bounds(int *status, void *stream) {
+  if (!status) return W4A16_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(status) & 3u) return W4A16_ERR_MISALIGNED;
+  int *err = device_error_word();
+  if (!err) return W4A16_ERR_CUDA;
+  return map_launch(launch_bounds_selftest(status, err, static_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_set_option(int option, int value) {

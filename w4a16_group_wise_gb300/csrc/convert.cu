@@ -14,6 +14,7 @@
 // octet as 32 contiguous bytes.  qzeros: one thread per word permutes its nibbles.
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "kernels.h"
 
 namespace w4a16 {
@@ -22,14 +23,18 @@ namespace {
 __device__ __forceinline__ int awq_slot(int o) { return (o & 1) ? 4 + (o >> 1) : (o >> 1); }
 
 __global__ void __launch_bounds__(256) awq_to_standard_q_kernel(const int32_t *__restrict__ qa, int K, int N,
-                                                                int32_t *__restrict__ qs) {
+                                                                int32_t *__restrict__ qs, int *err) {
+  const long long ext = 4LL * (K / 8) * N;  // both tensors: K*N/8 words
   const int C = N / 8;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row octet r, word column c)
   if (i >= (int64_t)(K / 8) * C) return;
   const int r = (int)(i / C), c = (int)(i % C);
   uint32_t in[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) in[j] = (uint32_t)__ldg(qa + (int64_t)(8 * r + j) * C + c);
+  for (int j = 0; j < 8; ++j) {
+    const int32_t *src = qa + (int64_t)(8 * r + j) * C + c;
+    in[j] = in_extent(src, 4, qa, ext, err) ? (uint32_t)__ldg(src) : 0u;
+  }
   uint32_t out[8];
 #pragma unroll
   for (int o = 0; o < 8; ++o) {  // column 8c + o: its nibble of rows 8r .. 8r+7
@@ -40,14 +45,16 @@ __global__ void __launch_bounds__(256) awq_to_standard_q_kernel(const int32_t *_
     out[o] = w;
   }
   uint4 *dst = reinterpret_cast<uint4 *>(qs + (int64_t)r * N + 8 * c);  // 32 contiguous bytes
+  if (!in_extent(dst, 32, qs, ext, err)) return;
   dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
   dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
 __global__ void __launch_bounds__(256) awq_to_standard_z_kernel(const int32_t *__restrict__ za, int64_t words,
-                                                                int32_t *__restrict__ zs) {
+                                                                int32_t *__restrict__ zs, int *err) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= words) return;
+  if (!in_extent(za + i, 4, za, 4 * words, err) || !in_extent(zs + i, 4, zs, 4 * words, err)) return;
   const uint32_t src = (uint32_t)__ldg(za + i);
   uint32_t w = 0;
 #pragma unroll
@@ -58,12 +65,12 @@ __global__ void __launch_bounds__(256) awq_to_standard_z_kernel(const int32_t *_
 }  // namespace
 
 cudaError_t launch_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N,
-                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std,
+                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std, int *err,
                                    cudaStream_t stream) {
   const int64_t qthreads = (int64_t)(K / 8) * (N / 8), zwords = (int64_t)zero_rows * (N / 8);
-  awq_to_standard_q_kernel<<<(unsigned)((qthreads + 255) / 256), 256, 0, stream>>>(qweight_awq, K, N, qweight_std);
+  awq_to_standard_q_kernel<<<(unsigned)((qthreads + 255) / 256), 256, 0, stream>>>(qweight_awq, K, N, qweight_std, err);
   if (zwords > 0)
-    awq_to_standard_z_kernel<<<(unsigned)((zwords + 255) / 256), 256, 0, stream>>>(qzeros_awq, zwords, qzeros_std);
+    awq_to_standard_z_kernel<<<(unsigned)((zwords + 255) / 256), 256, 0, stream>>>(qzeros_awq, zwords, qzeros_std, err);
   return cudaGetLastError();
 }
 

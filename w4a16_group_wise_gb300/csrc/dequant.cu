@@ -10,6 +10,7 @@
 // converted into a shared [128 k][64 n] tile, then written out as 16-byte row segments.
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "dq.cuh"
 #include "kernels.h"
 #include "layout.cuh"
@@ -27,21 +28,25 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
   const int b = blockIdx.x, t = blockIdx.y;
   const int CB = chunk_bytes(g);
   const uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + t) * CB;
+  const long long pext = packed_extent(K, N, g), wext = 2LL * K * N;
 
   if (threadIdx.x == 0) {
     const Header *h = reinterpret_cast<const Header *>(packed);
-    bad = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g ||
+    bad = (!in_extent(h, sizeof(Header), packed, pext, err) || h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g ||
            h->dtype != T::kDtype);
     if (bad) atomicOr(err, 1);
   }
 
   for (int u = threadIdx.x; u < kBlockN * 4; u += blockDim.x) {
     const int r = u % kBlockN, span = u / kBlockN;  // column-row, 32-k span
-    uint4 c = __ldg(reinterpret_cast<const uint4 *>(chunk + r * kRowBytes + span * 16));
+    const uint8_t *cp = chunk + r * kRowBytes + span * 16;
+    uint4 c = in_extent(cp, 16, packed, pext, err) ? __ldg(reinterpret_cast<const uint4 *>(cp)) : make_uint4(0, 0, 0, 0);
     const uint8_t *meta = chunk + kCodeBytes + ((32 * span) / g) * kGroupMetaBytes;
     const int p = meta_pos(r);
-    uint32_t s = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
-    uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
+    const uint16_t *sp = reinterpret_cast<const uint16_t *>(meta) + p;
+    const uint32_t *zp = reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8;
+    uint32_t s = in_extent(sp, 2, packed, pext, err) ? __ldg(sp) : 0u;
+    uint32_t zw = in_extent(zp, 4, packed, pext, err) ? __ldg(zp) : 0u;
     ZeroBias zb = T::zb((zw >> (4 * (p % 8))) & 0xFu);
     uint32_t s2 = s * 0x00010001u;
     uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -65,7 +70,7 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict_
   for (int i = threadIdx.x; i < kTileK * (kBlockN / 8); i += blockDim.x) {
     const int kk = i / (kBlockN / 8), v = i % (kBlockN / 8);
     const int k = kb + kk, n = b * kBlockN + 8 * v;
-    if (k < K && n < N)
+    if (k < K && n < N && in_extent(W + (size_t)k * N + n, 16, W, wext, err))
       *reinterpret_cast<uint4 *>(W + (size_t)k * N + n) = *reinterpret_cast<const uint4 *>(&tile[kk][8 * v]);
   }
 }

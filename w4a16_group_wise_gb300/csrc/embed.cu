@@ -15,6 +15,7 @@
 // bytes.  An id outside [0, N) gives a row of zeros and records a device-side error.
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "dq.cuh"
 #include "kernels.h"
 #include "layout.cuh"
@@ -33,31 +34,36 @@ __global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const int32_t *__r
   const int c = blockIdx.y * kChunksPerCta + threadIdx.x / 16;  // chunk (k-tile) of this thread
   const int w = threadIdx.x % 16;                                // code word of the column row
   const int k0 = c * kTileK + 8 * w;
+  const int ntok = gridDim.x;  // tokens: one CTA row per id
+  const long long pext = packed_extent(K, N, g), oext = 2LL * ntok * K;
   const Header *h = reinterpret_cast<const Header *>(packed);
-  const bool hdr_ok = h->magic == kMagic && h->version == kLayoutVersion && h->K == K && h->N == N && h->g == g &&
+  const bool hdr_ok = in_extent(h, sizeof(Header), packed, pext, err) && h->magic == kMagic && h->version == kLayoutVersion && h->K == K && h->N == N && h->g == g &&
                       h->dtype == T::kDtype;
   if (!hdr_ok) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, 1);
     return;  // a mismatched buffer writes nothing
   }
   if (c >= KT || k0 >= K) return;
-  const int n = __ldg(ids + t);
+  const int n = in_extent(ids + t, 4, ids, 4LL * ntok, err) ? __ldg(ids + t) : 0;
   uint4 o = make_uint4(0, 0, 0, 0);
   if (n < 0 || n >= N) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, 4);
   } else {
     const int b = n / kBlockN, rr = n % kBlockN, p = meta_pos(rr);
     const uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + c) * chunk_bytes(g);
-    const uint32_t word = __ldg(reinterpret_cast<const uint32_t *>(chunk + rr * kRowBytes) + w);
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(chunk + rr * kRowBytes) + w;
     const uint8_t *meta = chunk + kCodeBytes + ((8 * w) / g) * kGroupMetaBytes;
-    const uint32_t s = __ldg(reinterpret_cast<const uint16_t *>(meta) + p);
-    const uint32_t zw = __ldg(reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8);
+    const uint16_t *sp = reinterpret_cast<const uint16_t *>(meta) + p;
+    const uint32_t *zp = reinterpret_cast<const uint32_t *>(meta + kScaleBytes) + p / 8;
+    const uint32_t word = in_extent(wp, 4, packed, pext, err) ? __ldg(wp) : 0u;
+    const uint32_t s = in_extent(sp, 2, packed, pext, err) ? __ldg(sp) : 0u;
+    const uint32_t zw = in_extent(zp, 4, packed, pext, err) ? __ldg(zp) : 0u;
     uint32_t v[4];
     T::qz(word, T::zb((zw >> (4 * (p % 8))) & 0xFu), v);
     const uint32_t s2 = s * 0x00010001u;
     o = make_uint4(T::mul2(v[0], s2), T::mul2(v[1], s2), T::mul2(v[2], s2), T::mul2(v[3], s2));
   }
-  *reinterpret_cast<uint4 *>(out + (size_t)t * K + k0) = o;
+  if (in_extent(out + (size_t)t * K + k0, 16, out, oext, err)) *reinterpret_cast<uint4 *>(out + (size_t)t * K + k0) = o;
 }
 
 }  // namespace

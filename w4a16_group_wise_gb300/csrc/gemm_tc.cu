@@ -51,6 +51,7 @@
 #include "../../include/w4a16.h"
 
 #include "dq.cuh"
+#include "bounds.cuh"
 #include "kernels.h"
 #include "layout.cuh"
 #include "ptx.cuh"
@@ -222,6 +223,7 @@ struct SplitPlan {
   int stages_per_split;  // 128-k stages per split (the last split may have fewer)
   float *partials;       // [splits][tiles][bm][128] fp32
   int *counters;         // [tiles], zero between calls
+  long long partial_bytes;  // extent of `partials` (the bounds-checked build checks against it)
 };
 
 // Cluster split-K reduction of one CTA's pieces [e0, e1) of the tile (float4 pieces, 32 per row
@@ -230,7 +232,7 @@ struct SplitPlan {
 // pieces per thread in flight.
 template <class T, int S, int U>
 __device__ __forceinline__ void cluster_reduce(const float *part, int e0, int e1, int m0, int n0, int M, int N,
-                                               uint16_t *__restrict__ y) {
+                                               uint16_t *__restrict__ y, int *err) {
   uint32_t base[S];
 #pragma unroll
   for (int z = 0; z < S; ++z) base[z] = mapa_shared(part, (uint32_t)z);
@@ -258,7 +260,7 @@ __device__ __forceinline__ void cluster_reduce(const float *part, int e0, int e1
         acc.w += v[u][z].w;
       }
       const int gm = m0 + (eu >> 5), gn = n0 + 4 * (eu & 31);
-      if (gm < M && gn < N) {
+      if (gm < M && gn < N && in_extent(y + (size_t)gm * N + gn, 8, y, 2LL * M * N, err)) {
         uint2 o;
         o.x = T::pack2(acc.x, acc.y);
         o.y = T::pack2(acc.z, acc.w);
@@ -287,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const GemmSmem L = gemm_smem(bm, stages);
   const int NB = num_nblocks(N);
   const int CB = chunk_bytes(g);
+  // buffer extents in bytes, for the bounds-checked build (x is read by TMA only, through a tensor
+  // map of extent M x K: the copy engine fills coordinates outside it and reads nothing there)
+  const long long pext = packed_extent(K, N, g), yext = 2LL * M * N;
   const int KS = KT;  // 128-k stages over K: one per chunk (k past K reads as 0 and has code 0)
   const int st_begin = blockIdx.z * sp.stages_per_split;
   const int nst = max(0, min(KS, st_begin + sp.stages_per_split) - st_begin);
@@ -320,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     mbar_init(&accum_bar, 1);
     // the packed buffer must match the call (read-only: no need to wait for the previous kernel)
     const Header *h = reinterpret_cast<const Header *>(packed);
-    flags = (h->magic != kMagic || h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g ||
-             h->dtype != T::kDtype) ? 1 : 0;
+    flags = (!in_extent(h, sizeof(Header), packed, pext, err) || h->magic != kMagic ||
+             h->version != kLayoutVersion || h->K != K || h->N != N || h->g != g || h->dtype != T::kDtype) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {  // the whole warp allocates tensor memory: tmem_cols fp32 columns x 128 lanes
@@ -427,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (lane == 0) {
       auto chunk_src = [&](int it, int lc, int q) {
         const int nb0 = tile_n0(it) >> 6;
-        return packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + st_begin + lc) * CB;
+        const uint8_t *src = packed + kHeaderBytes + ((size_t)(nb0 + q) * KT + st_begin + lc) * CB;
+        return in_extent(src, CB, packed, pext, err) ? src : packed;  // a miss still completes the barrier
       };
       auto nblocks = [&](int it) { return ((tile_n0(it) >> 6) + 1 < NB) ? 2 : 1; };
       bool ok = true;
@@ -601,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           for (int hq = 0; hq < 2; ++hq) {  // 64 pieces of 8 n: (m = piece / 4, n = 8 * (piece % 4))
             const int pc = lane + 32 * hq, j2 = pc >> 2, nn = 8 * (pc & 3);
             const int m = m0 + c00 + 16 * b + j2, n = n0 + nn;
-            if (store && m < M && n < N)
+            if (store && m < M && n < N && in_extent(y + (size_t)m * N + n, 16, y, yext, err))
               *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
           }
           __syncwarp();
@@ -666,13 +672,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       // pieces in flight per thread: 16 loads whatever the split count (measured: two pieces per
       // thread, four round trips at two splits, took ~5,600 cycles per 256-row tile)
       switch (sp.splits) {
-        case 2: cluster_reduce<T, 2, 8>(part, e0, e1, m0, n0, M, N, y); break;
-        case 3: cluster_reduce<T, 3, 5>(part, e0, e1, m0, n0, M, N, y); break;
-        case 4: cluster_reduce<T, 4, 4>(part, e0, e1, m0, n0, M, N, y); break;
-        case 5: cluster_reduce<T, 5, 3>(part, e0, e1, m0, n0, M, N, y); break;
-        case 6: cluster_reduce<T, 6, 2>(part, e0, e1, m0, n0, M, N, y); break;
-        case 7: cluster_reduce<T, 7, 2>(part, e0, e1, m0, n0, M, N, y); break;
-        default: cluster_reduce<T, 8, 2>(part, e0, e1, m0, n0, M, N, y); break;
+        case 2: cluster_reduce<T, 2, 8>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 3: cluster_reduce<T, 3, 5>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 4: cluster_reduce<T, 4, 4>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 5: cluster_reduce<T, 5, 3>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 6: cluster_reduce<T, 6, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 7: cluster_reduce<T, 7, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
+        default: cluster_reduce<T, 8, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
       }
     }
     cluster_arrive();  // no CTA leaves while another still reads its partial
@@ -690,15 +696,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // 128 pieces of 4 floats: (m = piece / 8, n = 4 * (piece % 8))
           const int pc = lane + 32 * q, j2 = pc >> 3, nn = 4 * (pc & 7);
-          __stcg(reinterpret_cast<float4 *>(mine + (size_t)(c0 + j2) * kBN + 32 * quarter + nn),
-                 *reinterpret_cast<const float4 *>(tb + (j2 * 32 + nn) * 4));
+          float *dst = mine + (size_t)(c0 + j2) * kBN + 32 * quarter + nn;
+          if (in_extent(dst, 16, sp.partials, sp.partial_bytes, err))
+            __stcg(reinterpret_cast<float4 *>(dst), *reinterpret_cast<const float4 *>(tb + (j2 * 32 + nn) * 4));
         }
         __syncwarp();
       }
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) last = (atomicAdd(&sp.counters[tile], 1) == sp.splits - 1);
+    if (threadIdx.x == 0)
+      last = in_extent(&sp.counters[tile], 4, sp.counters, (long long)kSplitCounterBytes, err) &&
+             (atomicAdd(&sp.counters[tile], 1) == sp.splits - 1);
     __syncthreads();
     if (!last) {
       fl = 0;  // errors are reported by the last CTA of the tile
@@ -719,15 +728,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int pc = lane + 32 * q, j2 = pc >> 3, nn = 4 * (pc & 7);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int z = 0; z < sp.splits; ++z) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-              sp.partials + (((size_t)z * tiles + tile) * bm + c0 + j2) * kBN + 32 * quarter + nn));
+          const float *src = sp.partials + (((size_t)z * tiles + tile) * bm + c0 + j2) * kBN + 32 * quarter + nn;
+          const float4 v = in_extent(src, 16, sp.partials, sp.partial_bytes, err)
+                               ? __ldcg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
           acc.w += v.w;
         }
         const int m = m0 + c0 + j2, n = nq + nn;
-        if (m < M && n < N) {
+        if (m < M && n < N && in_extent(y + (size_t)m * N + n, 8, y, yext, err)) {
           uint2 o;
           o.x = T::pack2(acc.x, acc.y);
           o.y = T::pack2(acc.z, acc.w);
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
           const int pc = lane + 32 * q, j2 = pc >> 2, nn = 8 * (pc & 3);
           const int m = m0 + c0 + j2, n = nq + nn;
-          if (m < M && n < N)
+          if (m < M && n < N && in_extent(y + (size_t)m * N + n, 16, y, yext, err))
             *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
         }
         __syncwarp();
@@ -980,6 +990,7 @@ cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *pac
   const bool global = P.partial_bytes > 0;
   sp.counters = global ? static_cast<int *>(workspace) : nullptr;
   sp.partials = global ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
+  sp.partial_bytes = (long long)P.partial_bytes;
 
   static std::atomic<bool> configured[64];  // per device: the attribute has been set
   int dev = 0;

@@ -45,6 +45,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "bounds.cuh"
 #include "dq.cuh"
 #include "kernels.h"
 #include "layout.cuh"
@@ -71,6 +72,26 @@ __device__ __forceinline__ uint32_t ld_stream1(const void *p) {
   uint16_t v;
   asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
+}
+
+// The loads of the packed weights, through the debug build's bounds check (bounds.cuh): pext is
+// the packed buffer's extent in bytes.
+__device__ __forceinline__ uint4 ld_w16(const uint8_t *p, const uint8_t *packed, long long pext, int *err) {
+  return in_extent(p, 16, packed, pext, err) ? ld_stream16(p) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ uint32_t ld_w4(const uint8_t *p, const uint8_t *packed, long long pext, int *err) {
+  return in_extent(p, 4, packed, pext, err) ? ld_stream4(p) : 0u;
+}
+__device__ __forceinline__ uint32_t ld_w1(const uint8_t *p, const uint8_t *packed, long long pext, int *err) {
+  return in_extent(p, 1, packed, pext, err) ? ld_stream1(p) : 0u;
+}
+// The header check of a kernel (thread 0): the buffer describes this layer.
+template <class T>
+__device__ __forceinline__ int header_ok(const uint8_t *packed, int K, int N, int g, long long pext, int *err) {
+  if (!in_extent(packed, sizeof(Header), packed, pext, err)) return 0;
+  const Header *h = reinterpret_cast<const Header *>(packed);
+  return (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
+         (h->dtype == T::kDtype);
 }
 
 // What one lane holds for one chunk of weights.
@@ -112,12 +133,9 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
   const uint8_t *body = packed + kHeaderBytes + (size_t)b * KT * CB;
   const int mine = (KT - warp + W - 1) / W;  // chunks warp, warp + W, ...
 
+  const long long pext = packed_extent(K, N, g), xext = 2LL * M * K, yext = 2LL * M * N;
   int hdr_ok = 1;
-  if (threadIdx.x == 0) {
-    const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
-    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
-             (h->dtype == T::kDtype);
-  }
+  if (threadIdx.x == 0) hdr_ok = header_ok<T>(packed, K, N, g, pext, err);  // checked at the end
 
   auto load_w = [&](Stage<RT> &st, int j) {
     const uint8_t *ch = body + (size_t)(warp + j * W) * CB;
@@ -126,9 +144,10 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
     for (int r = 0; r < RT; ++r) {
       const int i = i0 + r;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) st.code[r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
-      st.scale[r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
-      st.zero[r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+      for (int h = 0; h < 2; ++h)
+        st.code[r][h] = ld_w16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t, packed, pext, err);
+      st.scale[r] = ld_w4(meta + 2 * (8 * r8 + 2 * i), packed, pext, err);
+      st.zero[r] = ld_w1(meta + kScaleBytes + 4 * r8 + i, packed, pext, err);
     }
   };
   auto load_x = [&](XFrag<MB> &xf, int j) {
@@ -136,7 +155,7 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 #pragma unroll
     for (int mb = 0; mb < MB; ++mb) {
       const int m = m0 + 8 * mb + r8;
-      const bool in = (m < M) && (kx < K);
+      const bool in = (m < M) && (kx < K) && in_extent(x + (size_t)m * K + kx, 64, x, xext, err);
       const uint4 *xp = reinterpret_cast<const uint4 *>(x + (size_t)(in ? m : 0) * K + (in ? kx : 0));
 #pragma unroll
       for (int q = 0; q < 4; ++q) xf.v[mb][q] = in ? __ldg(xp + q) : make_uint4(0, 0, 0, 0);
@@ -239,7 +258,7 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
     const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = m0 + 8 * mb + 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
-    if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
+    if (m < M && n < N && in_extent(y + (size_t)m * N + n, 2, y, yext, err)) y[(size_t)m * N + n] = T::from_float(v);
   }
 }
 
@@ -313,12 +332,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
   const uint8_t *body = packed + kHeaderBytes + (size_t)b * KT * CB;
   const int mine = (KT - warp + kSmallWarps - 1) / kSmallWarps;  // chunks warp, warp + 8, ...
 
+  const long long pext = packed_extent(K, N, g), xext = 2LL * M * K, yext = 2LL * M * N;
   int hdr_ok = 1;
-  if (threadIdx.x == 0) {
-    const Header *h = reinterpret_cast<const Header *>(packed);  // checked at the end
-    hdr_ok = (h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
-             (h->dtype == T::kDtype);
-  }
+  if (threadIdx.x == 0) hdr_ok = header_ok<T>(packed, K, N, g, pext, err);  // checked at the end
 
   uint4 code[D][RT][2];
   uint32_t scale[D][RT], zero[D][RT];
@@ -329,9 +345,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
     for (int r = 0; r < RT; ++r) {
       const int i = i0 + r;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) code[d][r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
-      scale[d][r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
-      zero[d][r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+      for (int h = 0; h < 2; ++h)
+        code[d][r][h] = ld_w16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t, packed, pext, err);
+      scale[d][r] = ld_w4(meta + 2 * (8 * r8 + 2 * i), packed, pext, err);
+      zero[d][r] = ld_w1(meta + kScaleBytes + 4 * r8 + i, packed, pext, err);
     }
   };
   // x rows 0..M-1 of chunk j into slot d: M * 16 pieces of 16 bytes, lane p takes pieces p, p+32..
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
     const int k0 = (warp + j * kSmallWarps) * kTileK;
     for (int p = lane; p < M * 16; p += 32) {
       const int m = p / 16, q = p % 16;
-      const bool ok = k0 + 8 * q < K;
+      const bool ok = k0 + 8 * q < K && in_extent(x + (size_t)m * K + k0 + 8 * q, 16, x, xext, err);
       cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
     }
   };
@@ -397,7 +414,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
     const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
     const int m = 2 * (ln & 3) + (c & 1);
     const int n = b * kBlockN + row;
-    if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
+    if (m < M && n < N && in_extent(y + (size_t)m * N + n, 2, y, yext, err)) y[(size_t)m * N + n] = T::from_float(v);
   }
 }
 
@@ -423,10 +440,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
   const int CB = chunk_bytes(g);
   const int mine = (KT - warp + kSmallWarps - 1) / kSmallWarps;  // chunks warp, warp + 8 (KT <= 16)
 
+  const long long pext = packed_extent(K, N, g), xext = 2LL * M * K, yext = 2LL * M * N;
   if (threadIdx.x == 0) {
-    const Header *h = reinterpret_cast<const Header *>(packed);
-    bad = !((h->magic == kMagic) & (h->version == kLayoutVersion) & (h->K == K) & (h->N == N) & (h->g == g) &
-            (h->dtype == T::kDtype));
+    bad = !header_ok<T>(packed, K, N, g, pext, err);
     if (bad && blockIdx.x == 0) atomicOr(err, 1);
   }
   __syncthreads();
@@ -442,9 +458,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
     for (int r = 0; r < RT; ++r) {
       const int i = i0 + r;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) code[d][r][h] = ld_stream16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t);
-      scale[d][r] = ld_stream4(meta + 2 * (8 * r8 + 2 * i));
-      zero[d][r] = ld_stream1(meta + kScaleBytes + 4 * r8 + i);
+      for (int h = 0; h < 2; ++h)
+        code[d][r][h] = ld_w16(ch + (16 * i + r8 + 8 * h) * kRowBytes + 16 * t, packed, pext, err);
+      scale[d][r] = ld_w4(meta + 2 * (8 * r8 + 2 * i), packed, pext, err);
+      zero[d][r] = ld_w1(meta + kScaleBytes + 4 * r8 + i, packed, pext, err);
     }
   };
 
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
       const int k0 = (warp + d * kSmallWarps) * kTileK;
       for (int pp = lane; pp < M * 16; pp += 32) {
         const int m = pp / 16, q = pp % 16;
-        const bool ok = k0 + 8 * q < K;
+        const bool ok = k0 + 8 * q < K && in_extent(x + (size_t)m * K + k0 + 8 * q, 16, x, xext, err);
         cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
       }
     }
@@ -497,7 +514,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
       const int row = 16 * (i0 + r) + (ln >> 2) + 8 * (c >> 1);
       const int m = 2 * (ln & 3) + (c & 1);
       const int n = b * kBlockN + row;
-      if (m < M && n < N) y[(size_t)m * N + n] = T::from_float(v);
+      if (m < M && n < N && in_extent(y + (size_t)m * N + n, 2, y, yext, err)) y[(size_t)m * N + n] = T::from_float(v);
     }
     __syncthreads();  // red is rewritten by the next pair
   }

@@ -20,7 +20,7 @@ namespace w4a16 {
 // (gsrc == g, or gsrc == K for one group over all of K).
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
                           const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
-                          int n0, int n1, void *packed, cudaStream_t stream);
+                          int n0, int n1, void *packed, int *err, cudaStream_t stream);
 
 // packed -> W[K][N].
 cudaError_t launch_dequant(const void *packed, int K, int N, int g, int dtype, uint16_t *W, int *err,
@@ -59,12 +59,17 @@ cudaError_t launch_embed(const int32_t *ids, int T, const void *packed, int K, i
 // AWQ -> GPTQ-style standard packing: qweight [K/8][N] packed along K in plain order, qzeros
 // [zero_rows][N/8] in plain order along N.
 cudaError_t launch_awq_to_standard(const int32_t *qweight_awq, const int32_t *qzeros_awq, int K, int N,
-                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std,
+                                   int zero_rows, int32_t *qweight_std, int32_t *qzeros_std, int *err,
                                    cudaStream_t stream);
 
 // Forced timeout of the bounded waits: one thread waits (polling, then sleeping) on an mbarrier
 // that nothing arrives at, with the given limit; *status gets a bit per wait that gave up.
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int *status, int *err, cudaStream_t stream);
+
+// Whether this is the bounds-checked debug build (bounds.cuh), and a one-thread run of its check
+// on five fixed cases (bit i of *status: case i judged outside its buffer).
+bool bounds_checked();
+cudaError_t launch_bounds_selftest(int *status, int *err, cudaStream_t stream);
 
 // The packed layout's group size for a caller's g (32, 64 or 128; or one group over all of K,
 // g == K or g == -1, stored as the largest of 128, 64, 32 dividing K); 0 when unsupported.

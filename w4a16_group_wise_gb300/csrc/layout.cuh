@@ -41,6 +41,11 @@ __host__ __device__ inline int chunk_bytes(int g) { return kCodeBytes + (kTileK 
 __host__ __device__ inline int num_nblocks(int N) { return (N + kBlockN - 1) / kBlockN; }
 __host__ __device__ inline int num_ktiles(int K) { return (K + kTileK - 1) / kTileK; }
 
+// bytes of a packed buffer of a K x N layer with layout group size g (header included)
+__host__ __device__ inline long long packed_extent(int K, int N, int g) {
+  return kHeaderBytes + (long long)num_nblocks(N) * num_ktiles(K) * chunk_bytes(g);
+}
+
 // lane-order position of column-row r (0..63) inside a group's meta
 __host__ __device__ inline int meta_pos(int r) { return 8 * (r % 8) + 2 * (r / 16) + (r / 8) % 2; }
 

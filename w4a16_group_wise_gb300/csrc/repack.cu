@@ -11,6 +11,7 @@
 // size).  One CTA writes one self-contained chunk, so any n-range can be repacked on its own.
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "kernels.h"
 #include "layout.cuh"
 
@@ -26,12 +27,17 @@ __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 *
 __global__ void __launch_bounds__(256) repack_kernel(
     const int32_t *__restrict__ qweight, int64_t ldq, const int32_t *__restrict__ qzeros,
     int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
-    int n0, int b0, int KT, uint8_t *__restrict__ packed) {
+    int n0, int n1, int b0, int KT, uint8_t *__restrict__ packed, int *err) {
   const int b = b0 + blockIdx.x;  // n-block
   const int t = blockIdx.y;       // k-tile
   const int kb = t * kTileK;
   const int CB = chunk_bytes(g);
   uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + t) * CB;
+  // extents of the source slices (columns [n0, n1) at their row strides) and of `packed`, in bytes
+  const int Gs = K / gsrc;
+  const long long wq = (n1 - n0) / 8;
+  const long long qext = 4 * ((K - 1) * ldq + wq), zext = 4 * ((Gs - 1) * ldz + wq);
+  const long long sext = 2 * ((Gs - 1) * lds + (n1 - n0)), pext = packed_extent(K, N, g);
 
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kHeaderBytes / 4) {
     uint32_t v = 0;
@@ -44,7 +50,8 @@ __global__ void __launch_bounds__(256) repack_kernel(
       case 5: v = (uint32_t)dtype; break;
       default: v = 0;
     }
-    reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
+    if (in_extent(reinterpret_cast<uint32_t *>(packed) + threadIdx.x, 4, packed, pext, err))
+      reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
   }
 
   // The chunk's 128 x 8 AWQ words (rows past K and columns past N read as 0), a row's 8 words by 8
@@ -58,13 +65,15 @@ __global__ void __launch_bounds__(256) repack_kernel(
   for (int i = threadIdx.x; i < kTileK * 8; i += blockDim.x) {
     const int kk = i >> 3, c = i & 7;
     const int k = kb + kk, n = b * kBlockN + 8 * c;
-    in[kk][c] = (k < K && n < N) ? (uint32_t)__ldg(qweight + (int64_t)k * ldq + (n - n0) / 8) : 0u;
+    const int32_t *src = qweight + (int64_t)k * ldq + (n - n0) / 8;
+    in[kk][c] = (k < K && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
   }
   if (threadIdx.x < gpc * 8) {
     const int l = threadIdx.x >> 3, c = threadIdx.x & 7;
     const int grp = t * gpc + l, n = b * kBlockN + 8 * c;
     const int sg = (grp * g) / gsrc;
-    zin[l][c] = (grp < G && n < N) ? (uint32_t)__ldg(qzeros + (int64_t)sg * ldz + (n - n0) / 8) : 0u;
+    const int32_t *src = qzeros + (int64_t)sg * ldz + (n - n0) / 8;
+    zin[l][c] = (grp < G && n < N && in_extent(src, 4, qzeros, zext, err)) ? (uint32_t)__ldg(src) : 0u;
   }
   __syncthreads();
 
@@ -81,7 +90,8 @@ __global__ void __launch_bounds__(256) repack_kernel(
   __syncthreads();
   // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
   uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
-  for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x) codes[i] = out[i >> 4][i & 15];
+  for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x)
+    if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[i >> 4][i & 15];
 
   // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
   // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
@@ -90,8 +100,10 @@ __global__ void __launch_bounds__(256) repack_kernel(
     const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r, read in order
     const int grp = t * gpc + l, n = b * kBlockN + r;
     const int sg = (grp * g) / gsrc;
-    const uint16_t sv = (grp < G && n < N) ? scales[(int64_t)sg * lds + (n - n0)] : (uint16_t)0;
-    reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes)[meta_pos(r)] = sv;
+    const uint16_t *src = scales + (int64_t)sg * lds + (n - n0);
+    const uint16_t sv = (grp < G && n < N && in_extent(src, 2, scales, sext, err)) ? *src : (uint16_t)0;
+    uint16_t *dst = reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes) + meta_pos(r);
+    if (in_extent(dst, 2, packed, pext, err)) *dst = sv;
   }
   if (threadIdx.x < gpc * 8) {
     const int l = threadIdx.x >> 3, wi = threadIdx.x & 7;
@@ -101,7 +113,8 @@ __global__ void __launch_bounds__(256) repack_kernel(
       const int r = meta_row(8 * wi + j);
       o |= ((zin[l][r >> 3] >> (4 * awq_slot_of_col(r & 7))) & 0xFu) << (4 * j);
     }
-    reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes)[wi] = o;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes) + wi;
+    if (in_extent(dst, 4, packed, pext, err)) *dst = o;
   }
 }
 
@@ -109,13 +122,13 @@ __global__ void __launch_bounds__(256) repack_kernel(
 
 cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qzeros, int64_t ldz,
                           const uint16_t *scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
-                          int n0, int n1, void *packed, cudaStream_t stream) {
+                          int n0, int n1, void *packed, int *err, cudaStream_t stream) {
   int b0 = n0 / kBlockN;
   int b1 = (n1 + kBlockN - 1) / kBlockN;
   int KT = num_ktiles(K);
   dim3 grid(b1 - b0, KT);
-  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0,
-                                          b0, KT, static_cast<uint8_t *>(packed));
+  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0, n1,
+                                          b0, KT, static_cast<uint8_t *>(packed), err);
   return cudaGetLastError();
 }
 

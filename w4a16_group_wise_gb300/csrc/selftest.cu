@@ -10,6 +10,7 @@
 // weights from the tinygemm layout, not a copy", the paragraph on the benchmark harness).
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -28,7 +29,28 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns, int
   if (timed_out) atomicOr(err, 2);  // the kernels' timeout code
 }
 
+// The bounds check itself (bounds.cuh), on offsets from `base` that nothing dereferences: bit i of
+// *status is set when case i is judged outside its extent.  Cases 0-1 lie inside a 64-byte
+// buffer, cases 2-4 (one byte past the end, one before the start, a zero-length buffer) outside.
+__global__ void __launch_bounds__(32) bounds_check_kernel(int *status, int *err) {
+  if (threadIdx.x != 0) return;
+  const long long off[5] = {0, 48, 49, -1, 0}, bytes[5] = {16, 16, 16, 1, 1}, ext[5] = {64, 64, 64, 64, 0};
+  const char *base = reinterpret_cast<const char *>(status);
+  int out = 0;
+#pragma unroll
+  for (int i = 0; i < 5; ++i)
+    if (!in_extent(base + off[i], bytes[i], base, ext[i], err)) out |= 1 << i;
+  *status = out;
+}
+
 }  // namespace
+
+bool bounds_checked() { return kBoundsCheck; }
+
+cudaError_t launch_bounds_selftest(int *status, int *err, cudaStream_t stream) {
+  bounds_check_kernel<<<1, 32, 0, stream>>>(status, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int *status, int *err, cudaStream_t stream) {
   wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, status, err);
