@@ -589,13 +589,45 @@ cudaError_t launch_stream(int tiles, bool factor, const uint16_t *x, const uint8
                 : cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, false>, x, p, M, N, K, g, KT, units, y, err);
 }
 
+// Dynamic shared memory (unused) that caps a lean CTA at two per SM: more than a third of the
+// SM's shared memory, with the CTA's static shared memory and the per-CTA reservation counted.
+template <class K>
+size_t two_per_sm_pad(K kernel) {
+  static std::atomic<long long> pad[64];  // per device, 0 until computed (stored + 1)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 0;
+  long long v = pad[dev].load(std::memory_order_relaxed);
+  if (!v) {
+    int per_sm = 0, reserved = 0;
+    cudaFuncAttributes fa = {};
+    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    long long need = 0;
+    if (per_sm > 0 && cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
+      need = per_sm / 3 + 1024 - (long long)fa.sharedSizeBytes - reserved;
+      need = need < 0 ? 0 : ((need + 1023) / 1024) * 1024;
+      // static + dynamic above 48 KB needs the opt-in; without it, leave the grid as it is
+      if (need > 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need) != cudaSuccess) {
+        cudaGetLastError();
+        need = 0;
+      }
+    }
+    v = need + 1;
+    pad[dev].store(v, std::memory_order_relaxed);
+  }
+  return (size_t)(v - 1);
+}
+
 template <class T, int D, int RT>
 cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_t *p, int M, int N, int K, int g,
-                         int KT, uint16_t *y, int *err, cudaStream_t stream) {
+                         int KT, uint16_t *y, int *err, cudaStream_t stream, bool spread = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((tiles + RT - 1) / RT);
   cfg.blockDim = dim3(32 * kSmallWarps);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = !spread ? 0
+                         : factor ? two_per_sm_pad(gemv_small_kernel<T, D, RT, true>)
+                                  : two_per_sm_pad(gemv_small_kernel<T, D, RT, false>);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -623,7 +655,11 @@ cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, i
     // one-tile CTAs (4 per SM) while they fit in one wave; two-tile CTAs (3 per SM) beyond, so
     // that every CTA is resident and has issued all its weight loads when the wait ends; resident
     // streaming CTAs where two-tile CTAs would need more than two waves (K <= 2048)
-    if (ctas1 <= 4L * sm_count()) return launch_small<T, 2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
+    // When the grid is at most two CTAs per SM, they are held to two per SM: the block scheduler
+    // fills an SM before it moves on, so a grid this small would otherwise sit four deep on a
+    // third of the SMs (measured: the 192 CTAs of a 2048 x 3072 layer on 50 of 152 SMs).
+    if (ctas1 <= 4L * sm_count())
+      return launch_small<T, 2, 1>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream, ctas1 <= 2L * sm_count());
     if (KT <= 2 * kSmallWarps && ctas1 > 12L * sm_count())
       return launch_stream<T>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
     return launch_small<T, 2, 2>(tiles, factor, x, p, M, N, K, g, KT, y, err, stream);
