@@ -591,9 +591,10 @@ cudaError_t launch_stream(int tiles, bool factor, const uint16_t *x, const uint8
 
 // Dynamic shared memory (unused) that caps a lean CTA at two per SM: more than a third of the
 // SM's shared memory, with the CTA's static shared memory and the per-CTA reservation counted.
-template <class K>
-size_t two_per_sm_pad(K kernel) {
-  static std::atomic<long long> pad[64];  // per device, 0 until computed (stored + 1)
+template <class T, int D, int RT, bool FACTOR>
+size_t two_per_sm_pad() {
+  auto kernel = gemv_small_kernel<T, D, RT, FACTOR>;
+  static std::atomic<long long> pad[64];  // per kernel and device, 0 until computed (stored + 1)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 0;
@@ -625,9 +626,7 @@ cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((tiles + RT - 1) / RT);
   cfg.blockDim = dim3(32 * kSmallWarps);
-  cfg.dynamicSmemBytes = !spread ? 0
-                         : factor ? two_per_sm_pad(gemv_small_kernel<T, D, RT, true>)
-                                  : two_per_sm_pad(gemv_small_kernel<T, D, RT, false>);
+  cfg.dynamicSmemBytes = !spread ? 0 : factor ? two_per_sm_pad<T, D, RT, true>() : two_per_sm_pad<T, D, RT, false>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
