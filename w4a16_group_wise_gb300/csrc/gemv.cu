@@ -272,12 +272,25 @@ __global__ void __launch_bounds__(kThreadBound<RT, MB>) gemv_kernel(const uint16
 constexpr int kSmallRows = 8;   // rows of x per CTA in the lean variant: the 8 columns of the MMA's B
 constexpr int kSmallWarps = 8;
 
+// The x ring's layout.  A slot holds rows m < 8 of 128 k, 256 bytes a row, as 16 pieces of 8 k.
+// With SW (more than 4 rows of x), piece q of row m sits at q ^ (2 ((q >> 3) & 1) | (m & 1)): a
+// quarter-warp's reads (rows r8 of one parity pair, spans t = 0..3, one 8-k step) then hit 8
+// different 16-byte bank groups, where the plain layout puts all rows, and the spans t and t + 2,
+// on the same ones (measured: the 131072-column head at M = 8 took 33 us swizzled against 42).
+// With few rows the plain layout is kept: fewer lanes read, and the XOR costs issue slots in a
+// conversion that is issue-bound (the M = 1 step lost 12% with it).
+template <bool SW>
+__device__ __forceinline__ int xring_piece(int m, int q) {
+  return SW ? (q ^ ((2 * ((q >> 3) & 1)) | (m & 1))) : q;
+}
+
 // One chunk slot of a lean or streaming CTA: (q - z) * s * x of the lane's weights (RT row-tiles x
 // rows r8, r8 + 8 x its 32 k) into the MMA accumulators acc[RT][4]; xs: the lane's 32 k of x row
-// r8 in shared memory (zeros where xrow is false).
-template <class T, int RT, bool FACTOR>
+// r8 in shared memory (zeros where xrow is false), its 8-k step w at byte 16 w, or (16 w) ^ xc
+// in the swizzled layout.
+template <class T, int RT, bool FACTOR, bool SW>
 __device__ __forceinline__ void slot_mma(const uint4 (&code)[RT][2], const uint32_t (&scale)[RT],
-                                         const uint32_t (&zero)[RT], const uint8_t *xs, bool xrow,
+                                         const uint32_t (&zero)[RT], const uint8_t *xs, int xc, bool xrow,
                                          float (&acc)[RT][4]) {
 #pragma unroll
   for (int r = 0; r < RT; ++r) {
@@ -299,7 +312,8 @@ __device__ __forceinline__ void slot_mma(const uint4 (&code)[RT][2], const uint3
           v1[e] = T::mul2(v1[e], s21);
         }
       }
-      const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + 16 * w) : make_uint4(0, 0, 0, 0);
+      const uint4 xw = xrow ? *reinterpret_cast<const uint4 *>(xs + (SW ? ((16 * w) ^ xc) : 16 * w))
+                            : make_uint4(0, 0, 0, 0);
       float *dst = FACTOR ? dd : acc[r];
       T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
       T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
@@ -315,7 +329,7 @@ __device__ __forceinline__ void slot_mma(const uint4 (&code)[RT][2], const uint3
   }
 }
 
-template <class T, int D, int RT, bool FACTOR>
+template <class T, int D, int RT, bool FACTOR, bool SW>
 __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
     uint16_t *__restrict__ y, int *err) {
@@ -357,9 +371,11 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
     for (int p = lane; p < M * 16; p += 32) {
       const int m = p / 16, q = p % 16;
       const bool ok = k0 + 8 * q < K && in_extent(x + (size_t)m * K + k0 + 8 * q, 16, x, xext, err);
-      cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
+      cp_async16_zfill(&xring[warp][d][m * 256 + 16 * xring_piece<SW>(m, q)], ok ? x + (size_t)m * K + k0 + 8 * q : x,
+                       ok);
     }
   };
+  const int xc = 16 * ((2 * (t >> 1)) | (r8 & 1));  // this lane's swizzle of its 16-byte reads
 
   float acc[RT][4];
 #pragma unroll
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
       if (j < mine) {
         cp_async_wait_pending<D - 1>();  // this slot's x has landed (for this lane's pieces)
         __syncwarp();                     // ... and every lane's pieces are visible
-        slot_mma<T, RT, FACTOR>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], r8 < M, acc);
+        slot_mma<T, RT, FACTOR, SW>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], xc, r8 < M, acc);
         __syncwarp();  // every lane is done reading the slot before it is refilled
         if (j + D < mine) {
           load_w(d, j + D);
@@ -426,7 +442,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, RT == 1 ? 4 : 3) gemv_small_
 // fetched once into shared memory; a warp requests its weights of the next pair as soon as those
 // of the current pair are in registers, so the weight stream does not wait for a CTA to exit and
 // a new one to start.  The packed header is checked before any weight is read.
-template <class T, bool FACTOR>
+template <class T, bool FACTOR, bool SW>
 __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed, int M, int N, int K, int g, int KT,
     int units, uint16_t *__restrict__ y, int *err) {
@@ -478,10 +494,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
       for (int pp = lane; pp < M * 16; pp += 32) {
         const int m = pp / 16, q = pp % 16;
         const bool ok = k0 + 8 * q < K && in_extent(x + (size_t)m * K + k0 + 8 * q, 16, x, xext, err);
-        cp_async16_zfill(&xring[warp][d][m * 256 + 16 * q], ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
+        cp_async16_zfill(&xring[warp][d][m * 256 + 16 * xring_piece<SW>(m, q)],
+                         ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
       }
     }
   }
+  const int xc = 16 * ((2 * (t >> 1)) | (r8 & 1));
   cp_async_commit();
   cp_async_wait_pending<0>();
   __syncwarp();
@@ -496,7 +514,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
 #pragma unroll
     for (int d = 0; d < D; ++d) {
       if (d < mine) {
-        slot_mma<T, RT, FACTOR>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], r8 < M, acc);
+        slot_mma<T, RT, FACTOR, SW>(code[d], scale[d], zero[d], &xring[warp][d][r8 * 256 + 64 * t], xc, r8 < M, acc);
         if (un < units) load_w(d, un);  // the next pair's weights stream in meanwhile
       }
     }
@@ -585,15 +603,18 @@ cudaError_t launch_stream(int tiles, bool factor, const uint16_t *x, const uint8
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return factor ? cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, true>, x, p, M, N, K, g, KT, units, y, err)
-                : cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, false>, x, p, M, N, K, g, KT, units, y, err);
+  if (M > 4)
+    return factor ? cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, true, true>, x, p, M, N, K, g, KT, units, y, err)
+                  : cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, false, true>, x, p, M, N, K, g, KT, units, y, err);
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, true, false>, x, p, M, N, K, g, KT, units, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_stream_kernel<T, false, false>, x, p, M, N, K, g, KT, units, y, err);
 }
 
 // Dynamic shared memory (unused) that caps a lean CTA at two per SM: more than a third of the
 // SM's shared memory, with the CTA's static shared memory and the per-CTA reservation counted.
-template <class T, int D, int RT, bool FACTOR>
+template <class T, int D, int RT, bool FACTOR, bool SW>
 size_t two_per_sm_pad() {
-  auto kernel = gemv_small_kernel<T, D, RT, FACTOR>;
+  auto kernel = gemv_small_kernel<T, D, RT, FACTOR, SW>;
   static std::atomic<long long> pad[64];  // per kernel and device, 0 until computed (stored + 1)
   int dev = 0;
   cudaGetDevice(&dev);
@@ -626,15 +647,23 @@ cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((tiles + RT - 1) / RT);
   cfg.blockDim = dim3(32 * kSmallWarps);
-  cfg.dynamicSmemBytes = !spread ? 0 : factor ? two_per_sm_pad<T, D, RT, true>() : two_per_sm_pad<T, D, RT, false>();
+  // swizzled x ring: measured faster at M = 8 (gate_up 6.14 -> 6.0 us) but slower at M = 5
+  // (q_k_v 2.82 -> 3.07 us) in this kernel; the streaming kernel takes it from M = 5
+  const bool sw = M >= 8;
+  cfg.dynamicSmemBytes = !spread ? 0
+                         : factor ? (sw ? two_per_sm_pad<T, D, RT, true, true>() : two_per_sm_pad<T, D, RT, true, false>())
+                                  : (sw ? two_per_sm_pad<T, D, RT, false, true>() : two_per_sm_pad<T, D, RT, false, false>());
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, true>, x, p, M, N, K, g, KT, y, err)
-                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, false>, x, p, M, N, K, g, KT, y, err);
+  if (sw)
+    return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, true, true>, x, p, M, N, K, g, KT, y, err)
+                  : cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, false, true>, x, p, M, N, K, g, KT, y, err);
+  return factor ? cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, true, false>, x, p, M, N, K, g, KT, y, err)
+                : cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, false, false>, x, p, M, N, K, g, KT, y, err);
 }
 
 template <class T>
