@@ -44,8 +44,8 @@ METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate
 # captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch each of q_k_v, gate_up
 # and down at M=1, summarised under profiles/), keyed by the sha256 of the kernel source they
 # were taken on; reported as null whenever that source has changed since.
-TRAFFIC = {"source_sha256": "502c65800c8c9132ffc889669dab283bd26f476d7d30d5e5940dcc60369cb662",
-           "bytes_per_launch": (3299328 + 14200064 + 7119872) // 3}
+TRAFFIC = {"source_sha256": "02ab5e39275a87e04b9ef6d81250fbd944049721c2a0eae65adefb4407090c4c",
+           "bytes_per_launch": (3299584 + 14200576 + 7119872) // 3}
 
 
 def max_over_ranks(ms, world, device):
