@@ -188,8 +188,26 @@ def test_gemm_decode_shapes_between_the_layers(K, N, M, g):
     assert w4.last_device_error() == 0
 
 
+@pytest.mark.parametrize("K,N,g", [(2048, 3072, 128), (2048, 3072, 32), (2048, 13312, 128), (4096, 2440, 64),
+                                   (2048, 80, 32)])
+def test_gemm_swizzled_x_ring_m8(K, N, g):
+    """M = 8 takes the lean kernel's swizzled x ring (one-tile CTAs at N = 3072, 2440 and 80, two-tile
+    CTAs at N = 13312), with the scale per chunk (g = 128) and per weight (g = 32, 64); M = 7 takes
+    the plain ring.  Every output against the oracle."""
+    L = Layer(K, N, g, seed=K + N + g)
+    x = inputs.make_x(8, K, seed=g)
+    _, y16 = L.ref(x)
+    y8 = L.gemm(x)
+    assert_close(y8, y16)
+    y7 = L.gemm(np.ascontiguousarray(x[:7]))
+    _, y16_7 = L.ref(np.ascontiguousarray(x[:7]))
+    assert_close(y7, y16_7)
+    assert w4.last_device_error() == 0
+
+
 @pytest.mark.parametrize("N,K,M,g", [(131072, 2048, 1, 64), (131072, 2048, 4, 128), (30000, 2048, 2, 128),
-                                     (30000, 2048, 3, 32), (30000, 320, 1, 64), (40000, 128, 2, 128)])
+                                     (30000, 2048, 3, 32), (30000, 320, 1, 64), (40000, 128, 2, 128),
+                                     (30000, 2048, 5, 128), (30000, 2048, 7, 32), (131072, 2048, 8, 64)])
 def test_gemm_streaming_decode_wide(N, K, M, g):
     """Decode of very wide layers (K <= 2048, more than 1824 row-tiles): resident CTAs walk pairs
     of row-tiles, prefetching the next pair's weights.  Sampled outputs against the oracle, the
@@ -261,7 +279,7 @@ def test_gemm_small_ragged(K, N, g, M):
     assert_close(L.gemm(x), y16)
 
 
-@pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 130])
+@pytest.mark.parametrize("M", [1, 4, 5, 8, 16, 17, 32, 33, 130])
 @pytest.mark.parametrize("g", [32, 128])
 def test_gemm_bit_exact_when_sums_are_exact(M, g):
     """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so the result must
