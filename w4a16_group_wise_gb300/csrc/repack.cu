@@ -8,7 +8,8 @@
 // "Motivacion de diseno").  This is the analogue of process_weights_after_loading: done once,
 // on the device, with no int32 expansion of the codes (vllm-omni commit "cpu_int4: repack
 // weights in n-blocks, to bound the load-time peak" measured that transient at 8x the packed
-// size).  One CTA writes one self-contained chunk, so any n-range can be repacked on its own.
+// size).  A CTA writes the chunks of four consecutive n-blocks of one k-tile, reading each AWQ row
+// as one 128-byte segment; chunks are self-contained, so any n-range can be repacked on its own.
 #include <cuda_runtime.h>
 
 #include "bounds.cuh"
@@ -24,15 +25,17 @@ __device__ __forceinline__ int awq_slot_of_col(int c) { return (c & 1) ? 4 + (c 
 // lane-order position p -> column-row r (inverse of meta_pos)
 __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 * (p % 2) + p / 8; }
 
+constexpr int kRepackBlocks = 4;  // n-blocks per CTA: 32 AWQ words = 128 contiguous bytes of a row
+
+// One CTA: kRepackBlocks consecutive n-blocks b0 + 4 blockIdx.x + bl (those below b1) of k-tile t.
 __global__ void __launch_bounds__(256) repack_kernel(
     const int32_t *__restrict__ qweight, int64_t ldq, const int32_t *__restrict__ qzeros,
     int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
-    int n0, int n1, int b0, int KT, uint8_t *__restrict__ packed, int *err) {
-  const int b = b0 + blockIdx.x;  // n-block
-  const int t = blockIdx.y;       // k-tile
+    int n0, int n1, int b0, int b1, int KT, uint8_t *__restrict__ packed, int *err) {
+  const int bfirst = b0 + kRepackBlocks * blockIdx.x;  // first n-block of this CTA
+  const int t = blockIdx.y;                            // k-tile
   const int kb = t * kTileK;
   const int CB = chunk_bytes(g);
-  uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + t) * CB;
   // extents of the source slices (columns [n0, n1) at their row strides) and of `packed`, in bytes
   const int Gs = K / gsrc;
   const long long wq = (n1 - n0) / 8;
@@ -54,67 +57,74 @@ __global__ void __launch_bounds__(256) repack_kernel(
       reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
   }
 
-  // The chunk's 128 x 8 AWQ words (rows past K and columns past N read as 0), a row's 8 words by 8
-  // consecutive threads (32 contiguous bytes); the row stride of 9 words keeps the reads of the
-  // transposition below free of bank conflicts.  Also the zero words of the chunk's groups.
-  const int gpc = kTileK / g;  // groups per chunk
+  // The 128 x 32 AWQ words of the CTA's n-blocks (rows past K, columns past N or past the last
+  // n-block read as 0): a warp reads one row's 128 contiguous bytes.  The row stride of 33 words
+  // keeps the transposition's reads free of bank conflicts.  Also the zero words of the groups.
+  constexpr int kW = 8 * kRepackBlocks;  // AWQ words of a row in this CTA
+  const int gpc = kTileK / g;            // groups per chunk
   const int G = K / g;
-  __shared__ uint32_t in[kTileK][9];
-  __shared__ uint32_t out[kBlockN][17];  // the chunk's code words (row stride 17: no bank conflicts)
-  __shared__ uint32_t zin[4][8];                         // [group of the chunk][AWQ zero word]
-  for (int i = threadIdx.x; i < kTileK * 8; i += blockDim.x) {
-    const int kk = i >> 3, c = i & 7;
-    const int k = kb + kk, n = b * kBlockN + 8 * c;
+  __shared__ uint32_t in[kTileK][kW + 1];
+  __shared__ uint32_t out[kRepackBlocks][kBlockN][17];  // code words per n-block (row stride 17)
+  __shared__ uint32_t zin[4][kW];                       // [group of the chunk][AWQ zero word]
+  for (int i = threadIdx.x; i < kTileK * kW; i += blockDim.x) {
+    const int kk = i / kW, c = i % kW;
+    const int k = kb + kk, b = bfirst + c / 8, n = b * kBlockN + 8 * (c % 8);
     const int32_t *src = qweight + (int64_t)k * ldq + (n - n0) / 8;
-    in[kk][c] = (k < K && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
+    in[kk][c] = (k < K && b < b1 && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
   }
-  if (threadIdx.x < gpc * 8) {
-    const int l = threadIdx.x >> 3, c = threadIdx.x & 7;
-    const int grp = t * gpc + l, n = b * kBlockN + 8 * c;
+  if (threadIdx.x < gpc * kW) {
+    const int l = threadIdx.x / kW, c = threadIdx.x % kW;
+    const int grp = t * gpc + l, b = bfirst + c / 8, n = b * kBlockN + 8 * (c % 8);
     const int sg = (grp * g) / gsrc;
     const int32_t *src = qzeros + (int64_t)sg * ldz + (n - n0) / 8;
-    zin[l][c] = (grp < G && n < N && in_extent(src, 4, qzeros, zext, err)) ? (uint32_t)__ldg(src) : 0u;
+    zin[l][c] = (grp < G && b < b1 && n < N && in_extent(src, 4, qzeros, zext, err)) ? (uint32_t)__ldg(src) : 0u;
   }
   __syncthreads();
 
-  // Codes: row r (column 64b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  Threads take r
+  // Codes: row r (column 64 b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  Threads take r
   // fastest, so a warp reads 4 distinct words per step (the rest are broadcasts).
-  for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x) {
-    const int r = i & (kBlockN - 1), w = i >> 6;
-    const int c = r >> 3, sh = 4 * awq_slot_of_col(r & 7);
+  for (int i = threadIdx.x; i < kRepackBlocks * kBlockN * 16; i += blockDim.x) {
+    const int r = i & (kBlockN - 1), w = (i >> 6) & 15, bl = i >> 10;
+    const int c = 8 * bl + (r >> 3), sh = 4 * awq_slot_of_col(r & 7);
     uint32_t o = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) o |= ((in[8 * w + slot_k(j)][c] >> sh) & 0xFu) << (4 * j);
-    out[r][w] = o;
+    out[bl][r][w] = o;
   }
   __syncthreads();
-  // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
-  uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
-  for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x)
-    if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[i >> 4][i & 15];
 
-  // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
-  // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
-  // source tensors (gsrc == g, or gsrc == K for one group over all of K).
-  for (int i = threadIdx.x; i < gpc * kBlockN; i += blockDim.x) {
-    const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r, read in order
-    const int grp = t * gpc + l, n = b * kBlockN + r;
-    const int sg = (grp * g) / gsrc;
-    const uint16_t *src = scales + (int64_t)sg * lds + (n - n0);
-    const uint16_t sv = (grp < G && n < N && in_extent(src, 2, scales, sext, err)) ? *src : (uint16_t)0;
-    uint16_t *dst = reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes) + meta_pos(r);
-    if (in_extent(dst, 2, packed, pext, err)) *dst = sv;
-  }
-  if (threadIdx.x < gpc * 8) {
-    const int l = threadIdx.x >> 3, wi = threadIdx.x & 7;
-    uint32_t o = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r = meta_row(8 * wi + j);
-      o |= ((zin[l][r >> 3] >> (4 * awq_slot_of_col(r & 7))) & 0xFu) << (4 * j);
+  for (int bl = 0; bl < kRepackBlocks; ++bl) {
+    const int b = bfirst + bl;
+    if (b >= b1) break;
+    uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + t) * CB;
+    // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
+    uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
+    for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x)
+      if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[bl][i >> 4][i & 15];
+
+    // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
+    // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
+    // source tensors (gsrc == g, or gsrc == K for one group over all of K).
+    for (int i = threadIdx.x; i < gpc * kBlockN; i += blockDim.x) {
+      const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r, read in order
+      const int grp = t * gpc + l, n = b * kBlockN + r;
+      const int sg = (grp * g) / gsrc;
+      const uint16_t *src = scales + (int64_t)sg * lds + (n - n0);
+      const uint16_t sv = (grp < G && n < N && in_extent(src, 2, scales, sext, err)) ? *src : (uint16_t)0;
+      uint16_t *dst = reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes) + meta_pos(r);
+      if (in_extent(dst, 2, packed, pext, err)) *dst = sv;
     }
-    uint32_t *dst = reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes) + wi;
-    if (in_extent(dst, 4, packed, pext, err)) *dst = o;
+    if (threadIdx.x < gpc * 8) {
+      const int l = threadIdx.x >> 3, wi = threadIdx.x & 7;
+      uint32_t o = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = meta_row(8 * wi + j);
+        o |= ((zin[l][8 * bl + (r >> 3)] >> (4 * awq_slot_of_col(r & 7))) & 0xFu) << (4 * j);
+      }
+      uint32_t *dst = reinterpret_cast<uint32_t *>(chunk + kCodeBytes + l * kGroupMetaBytes + kScaleBytes) + wi;
+      if (in_extent(dst, 4, packed, pext, err)) *dst = o;
+    }
   }
 }
 
@@ -126,9 +136,9 @@ cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qz
   int b0 = n0 / kBlockN;
   int b1 = (n1 + kBlockN - 1) / kBlockN;
   int KT = num_ktiles(K);
-  dim3 grid(b1 - b0, KT);
+  dim3 grid((b1 - b0 + kRepackBlocks - 1) / kRepackBlocks, KT);
   repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0, n1,
-                                          b0, KT, static_cast<uint8_t *>(packed), err);
+                                          b0, b1, KT, static_cast<uint8_t *>(packed), err);
   return cudaGetLastError();
 }
 
