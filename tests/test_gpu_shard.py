@@ -66,3 +66,19 @@ def test_slices_bit_exact_when_sums_are_exact(M):
     x = torch.from_numpy(xi).to(dev())
     y = torch.cat([p.forward(x) for p in _parts(L, 3)], dim=1).cpu().numpy().view(np.uint16)
     assert np.array_equal(y, y16)
+
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_bf16_slices_concatenate_to_the_whole_layer(M):
+    """The split of a bf16 layer: each rank's slice is repacked from the full bf16 scales and its
+    y meets the bf16 tolerance against the oracle's columns."""
+    from gpu_util import assert_close_bf16
+    K, N = inputs.SHAPES["qkv"]
+    L = Layer(K, N, 128, seed=24, dtype="bf16")
+    x_np = inputs.make_x(M, K, seed=M, dtype="bf16")
+    x = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).to(dev()).view(torch.bfloat16)
+    ys = [p.forward(x) for p in _parts(L, 3)]
+    assert all(y.dtype == torch.bfloat16 for y in ys)
+    y64, _ = L.ref(x_np)
+    assert_close_bf16(torch.cat(ys, dim=1), y64)
+    assert w4.last_device_error() == 0
