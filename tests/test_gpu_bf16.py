@@ -62,7 +62,7 @@ def test_bf16_chunked_repack_is_byte_identical():
 
 GEMM_CASES = [
     ("square", 1), ("qkv", 1), ("gate_up", 1), ("down", 1),
-    ("qkv", 3), ("gate_up", 16), ("down", 12), ("qkv", 8), ("gate_up", 8),
+    ("qkv", 3), ("gate_up", 16), ("down", 12), ("qkv", 8), ("gate_up", 8), ("qkv", 16), ("square", 10),
     ("qkv", 32), ("gate_up", 33), ("down", 40),
     ("qkv", 512), ("gate_up", 512), ("down", 512), ("square", 129),
 ]

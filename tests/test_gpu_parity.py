@@ -260,7 +260,7 @@ def test_gemm_persistent_ragged_sampled(name, M, g):
 
 
 @pytest.mark.parametrize("g", [32, 64, 128])
-@pytest.mark.parametrize("M", [1, 3, 17, 129])
+@pytest.mark.parametrize("M", [1, 3, 12, 17, 129])
 @pytest.mark.parametrize("zeros", ["sym8", "uniform"])
 def test_gemm_edge_tail(g, M, zeros):
     K, N = SHAPES["tail80"]
@@ -271,7 +271,8 @@ def test_gemm_edge_tail(g, M, zeros):
 
 
 @pytest.mark.parametrize("K,N,g,M", [(96, 8, 32, 5), (192, 72, 64, 2), (128, 64, 128, 1),
-                                     (224, 200, 32, 33), (4096, 264, 64, 16)])
+                                     (224, 200, 32, 33), (4096, 264, 64, 16), (2048, 200, 32, 13),
+                                     (224, 200, 32, 9), (2048, 13312, 128, 11), (1024, 2440, 64, 16)])
 def test_gemm_small_ragged(K, N, g, M):
     L = Layer(K, N, g, seed=7)
     x = inputs.make_x(M, K, seed=7)
@@ -279,7 +280,7 @@ def test_gemm_small_ragged(K, N, g, M):
     assert_close(L.gemm(x), y16)
 
 
-@pytest.mark.parametrize("M", [1, 4, 5, 8, 16, 17, 32, 33, 130])
+@pytest.mark.parametrize("M", [1, 4, 5, 8, 9, 12, 16, 17, 32, 33, 130])
 @pytest.mark.parametrize("g", [32, 128])
 def test_gemm_bit_exact_when_sums_are_exact(M, g):
     """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so the result must
