@@ -240,11 +240,14 @@ def test_streaming_decode_header_mismatch_writes_nothing():
 
 
 @pytest.mark.parametrize("name,M,g", [("gate_up", 300, 128), ("gate_up", 1000, 64), ("lm_head", 200, 32),
-                                     ("lm_head", 100, 128), ("lm_head", 150, 64), ("lm_head", 48, 32)])
+                                     ("lm_head", 100, 128), ("lm_head", 150, 64), ("lm_head", 48, 32),
+                                     ("gate_up", 777, 128), ("qkv", 1024, 128), ("qkv", 1023, 32)])
 def test_gemm_persistent_ragged_sampled(name, M, g):
     """Persistent tensor-core CTAs walking several tiles each, with a ragged last m-tile (and,
     for the LM head, hundreds of n-tiles per launch); checked on sampled outputs, every row m of
-    the last m-tile included.  At M <= 160 the CTAs alternate two accumulators tile by tile."""
+    the last m-tile included.  At M <= 160 the CTAs alternate two accumulators tile by tile.  An
+    odd M leaves the last row of a stored row pair alone; q_k_v at M = 1023/1024 takes one round
+    of 256-row tiles (96 CTAs)."""
     K, N = SHAPES[name]
     L = Layer(K, N, g, seed=M)
     x = inputs.make_x(M, K, seed=M)

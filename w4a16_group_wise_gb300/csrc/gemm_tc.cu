@@ -216,7 +216,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 struct SplitPlan {
   int splits;
   int cluster;           // 1: cluster reduction, 0: workspace reduction
-  int persist;           // 1: one CTA per SM walks the tiles (splits == 1)
   int dbl;               // 1: two accumulators, alternating by tile (persistent CTAs)
   int a_col0;            // first tensor-memory column of the stages' A tiles
   int ntn, ntm;          // n-tiles and m-tiles of the problem
@@ -270,7 +269,7 @@ __device__ __forceinline__ void cluster_reduce(const float *part, int e0, int e1
   }
 }
 
-template <class T>
+template <class T, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const uint8_t *__restrict__ packed, int M, int N,
                                                                int K, int g, int KT, int bm, int stages,
@@ -301,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   // (n-tile, m-tile) grid (m fastest, so neighbouring CTAs share weights); otherwise the one
   // tile (blockIdx.x, blockIdx.y).
   const int ntiles = sp.ntn * sp.ntm;
-  const int my_tiles = sp.persist ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  const int my_tiles = PERSIST ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 1;
   auto tile_n0 = [&](int it) {
-    return (sp.persist ? ((int)blockIdx.x + it * (int)gridDim.x) / sp.ntm : (int)blockIdx.x) * kBN;
+    return (PERSIST ? ((int)blockIdx.x + it * (int)gridDim.x) / sp.ntm : (int)blockIdx.x) * kBN;
   };
   auto tile_m0 = [&](int it) {
-    return (sp.persist ? ((int)blockIdx.x + it * (int)gridDim.x) % sp.ntm : (int)blockIdx.y) * bm;
+    return (PERSIST ? ((int)blockIdx.x + it * (int)gridDim.x) % sp.ntm : (int)blockIdx.y) * bm;
   };
 
   if (threadIdx.x == 0) {
@@ -392,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       for (int it = 0; it < my_tiles && ok; ++it) {
         // accumulator ab is free once the epilogue warps have read the last tile that used it
         const int ab = sp.dbl ? (it & 1) : 0, ause = sp.dbl ? (it >> 1) : it;
-        if (sp.persist && ause > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[ab], (ause - 1) & 1))) break;
+        if (PERSIST && ause > 0 && !(ok = mbar_wait_sleep_bounded(&tempty_bar[ab], (ause - 1) & 1))) break;
         tc_fence_after();
         const uint32_t acc = tmem + (uint32_t)(ab * bm);
         for (int j = 0; j < nst; ++j) {
@@ -416,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         if (!ok) break;
         // the accumulator is final once every MMA above completes
-        mma_commit(sp.persist ? &tfull_bar[ab] : &accum_bar);
+        mma_commit(PERSIST ? &tfull_bar[ab] : &accum_bar);
       }
       if (!ok) {  // let every issued MMA finish before the CTA may exit
         atomicOr(&flags, 2);
         mma_commit(&accum_bar);
         mbar_wait_sleep_bounded(&accum_bar, 0);
-      } else if (!sp.persist && !mbar_wait_sleep_bounded(&accum_bar, 0)) {
+      } else if (!PERSIST && !mbar_wait_sleep_bounded(&accum_bar, 0)) {
         atomicOr(&flags, 2);
       }
     }
@@ -573,13 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
     if (!ok) atomicOr(&flags, 2);
-  } else if (warp >= 4 + kDeqWarps && sp.persist) {
+  } else if (warp >= 4 + kDeqWarps && PERSIST) {
     // ------------------------------------------------------------ persistent epilogue
     // Warp q of the four reads TMEM lanes 32q .. 32q + 31 (column-rows n) of an accumulator
-    // (while the MMAs fill the other one, with two), 16 columns (rows m) at a time, rounds them
-    // and turns each 32 n x 16 m block around in its 1 KB of shared memory, so that a lane
-    // stores 16 bytes of consecutive n of one row m (measured: the 4-byte stores of lane pairs
-    // this replaces took ~9,000 cycles per 256-row tile while the MMAs waited).
+    // (while the MMAs fill the other one, with two), 16 columns (rows m) at a time, rounds each
+    // pair of rows into one fp16 pair and turns each 32 n x 16 m block around in its 1 KB of
+    // shared memory, so that a lane stores 16 bytes of consecutive n of two rows m (measured:
+    // the 4-byte stores of lane pairs this replaces took ~9,000 cycles per 256-row tile while the
+    // MMAs waited).  The accumulator is released as soon as its last columns are in registers,
+    // before they are stored (gate_up M = 512: 28.5 -> 26.7 us; M = 2048: 83 -> 78 us).
     const int q = warp & 3;
     uint16_t *th = reinterpret_cast<uint16_t *>(smem + L.epi_off + q * 1024);
     griddep_wait();  // y may still be read by the previous kernel
@@ -597,25 +598,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           if (c00 + 16 * b < bm)
             tmem_ld16_async(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * bm + c00 + 16 * b), v[b]);
         tmem_wait_ld();
+        if (c00 + 64 >= bm) {
+          // the whole accumulator is in registers: the MMAs may refill it while the last
+          // columns are stored
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[ab]);
+        }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           if (c00 + 16 * b >= bm) break;
+          // rows (2i, 2i + 1) of column-row n = lane as one fp16 pair, word n of row pair i (the
+          // odd pairs with the two 4-word halves of each 8 n swapped, so that the 16-byte reads
+          // below hit distinct banks)
+          uint32_t *tw = reinterpret_cast<uint32_t *>(th);
 #pragma unroll
-          for (int j2 = 0; j2 < 16; ++j2) th[j2 * 32 + lane] = T::from_float(__uint_as_float(v[b][j2]));
+          for (int i = 0; i < 8; ++i)
+            tw[i * 32 + (lane ^ (4 * (i & 1)))] = T::pack2(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1]));
           __syncwarp();
-#pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {  // 64 pieces of 8 n: (m = piece / 4, n = 8 * (piece % 4))
-            const int pc = lane + 32 * hq, j2 = pc >> 2, nn = 8 * (pc & 3);
-            const int m = m0 + c00 + 16 * b + j2, n = n0 + nn;
+          {  // lane: row pair i = lane / 4, n = 8 (lane % 4) .. + 7; rows 2i and 2i + 1 as 16-byte stores
+            const int i = lane >> 2, nn = 8 * (lane & 3), sw = 4 * (i & 1);
+            const uint4 a = *reinterpret_cast<const uint4 *>(tw + i * 32 + nn + sw);
+            const uint4 c = *reinterpret_cast<const uint4 *>(tw + i * 32 + nn + (sw ^ 4));
+            uint4 lo, hi;
+            lo.x = __byte_perm(a.x, a.y, 0x5410);
+            lo.y = __byte_perm(a.z, a.w, 0x5410);
+            lo.z = __byte_perm(c.x, c.y, 0x5410);
+            lo.w = __byte_perm(c.z, c.w, 0x5410);
+            hi.x = __byte_perm(a.x, a.y, 0x7632);
+            hi.y = __byte_perm(a.z, a.w, 0x7632);
+            hi.z = __byte_perm(c.x, c.y, 0x7632);
+            hi.w = __byte_perm(c.z, c.w, 0x7632);
+            const int m = m0 + c00 + 16 * b + 2 * i, n = n0 + nn;
             if (store && m < M && n < N && in_extent(y + (size_t)m * N + n, 16, y, yext, err))
-              *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
+              *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = lo;
+            if (store && m + 1 < M && n < N && in_extent(y + (size_t)(m + 1) * N + n, 16, y, yext, err))
+              *reinterpret_cast<uint4 *>(y + (size_t)(m + 1) * N + n) = hi;
           }
           __syncwarp();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[ab]);  // the MMAs may refill the accumulator
     }
     if (!ok) atomicOr(&flags, 2);
   }
@@ -627,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (sp.persist || !run) {
+  if (PERSIST || !run) {
     if (threadIdx.x == 0 && flags) atomicOr(err, flags);
   } else {
   griddep_wait();  // every storing thread waits for the previous kernel (a no-op once satisfied)
@@ -845,7 +867,7 @@ int max_clusters(int splits) {
   std::lock_guard<std::mutex> lock(mu);
   if (!cache[dev][splits]) {
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_tc_kernel<Fp16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<Fp16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, 1, splits);
       cfg.blockDim = dim3(kThreads);
@@ -857,7 +879,7 @@ int max_clusters(int splits) {
       attr[0].val.clusterDim.z = splits;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Fp16>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Fp16, false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     cache[dev][splits] = n > 0 ? n : -1;
@@ -876,13 +898,16 @@ TcPlan plan_gemm_tc(int M, int N, int K) {
   p.dbl = false;
   p.tmem_cols = kTmemCols;
   int tiles = ntn * ((M + p.bm - 1) / p.bm);
-  // Too few 256-row tiles to cover the GPU, but enough 128-row tiles to cover half of it: take the
-  // half-height tiles and no K split.  Measured at M = 512: q_k_v (48 tiles at BM = 256, two K
-  // splits) went from 14.4 to 13.2 us with 96 whole-K tiles; down (32 tiles, four splits) went
-  // from 19.5 to 21.5 us with 64 half-height tiles and two splits, so there BM stays 256.
+  // Too few 256-row tiles to cover the GPU, but enough 128-row tiles to cover half of it in one
+  // round: take the half-height tiles and no K split.  Measured at M = 512: q_k_v (48 tiles at
+  // BM = 256, two K splits) went from 14.4 to 13.2 us with 96 whole-K tiles; down (32 tiles, four
+  // splits) went from 19.5 to 21.5 us with 64 half-height tiles and two splits, so there BM stays
+  // 256.  A second round of half-height tiles costs more than it saves: a 128-row stage takes
+  // ~1300 cycles against ~1400 for 256 rows (q_k_v M = 1024: 20.9 us with 192 tiles of 128 rows,
+  // 15.4 us with 96 of 256).
   if (p.bm == 256 && 4 * tiles < 3 * sms) {
     const int tiles128 = ntn * ((M + 127) / 128);
-    if (2 * tiles128 >= sms) {
+    if (2 * tiles128 >= sms && tiles128 <= sms) {
       p.bm = 128;
       tiles = tiles128;
     }
@@ -982,7 +1007,6 @@ cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *pac
   sp.splits = P.splits;
   sp.cluster = P.cluster ? 1 : 0;
   sp.stages_per_split = P.stages_per_split;
-  sp.persist = P.persist ? 1 : 0;
   sp.dbl = P.dbl ? 1 : 0;
   sp.a_col0 = P.a_col0;
   sp.ntn = (N + kBN - 1) / kBN;
@@ -992,13 +1016,17 @@ cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *pac
   sp.partials = global ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes) : nullptr;
   sp.partial_bytes = (long long)P.partial_bytes;
 
-  static std::atomic<bool> configured[64];  // per device: the attribute has been set
+  // Persistent and split-K launches run separate instances of the kernel, each compiled without
+  // the other's epilogue (measured: with both in one function, adding work to the persistent
+  // epilogue slowed the split-K shapes by 1-3%).
+  auto kernel = P.persist ? gemm_tc_kernel<T, true> : gemm_tc_kernel<T, false>;
+  static std::atomic<bool> configured[2][64];  // per instance and device: the attribute has been set
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (dev >= 0 && dev < 64 && !configured[P.persist][dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
-    configured[dev].store(true, std::memory_order_release);
+    configured[P.persist][dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = P.persist ? dim3(std::min(P.tiles, sm_count_tc())) : dim3(sp.ntn, sp.ntm, P.splits);
@@ -1018,7 +1046,7 @@ cudaError_t launch_gemm_tc_t(const TcPlan &P, const uint16_t *x, const void *pac
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T>, map, static_cast<const uint8_t *>(packed), M, N, K, g,
+  return cudaLaunchKernelEx(&cfg, kernel, map, static_cast<const uint8_t *>(packed), M, N, K, g,
                             num_ktiles(K), P.bm, P.stages, P.tmem_cols, sp, y, err);
 }
 
