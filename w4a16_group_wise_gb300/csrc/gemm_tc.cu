@@ -414,14 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
         if (!ok) break;
-        // the accumulator is final once every MMA above completes
-        mma_commit(PERSIST ? &tfull_bar[ab] : &accum_bar);
+        // the accumulator is final once every MMA above completes; the CTA's last tile goes to
+        // all warps at the end, the others to the epilogue warps
+        mma_commit(PERSIST && it + 1 < my_tiles ? &tfull_bar[ab] : &accum_bar);
       }
       if (!ok) {  // let every issued MMA finish before the CTA may exit
         atomicOr(&flags, 2);
         mma_commit(&accum_bar);
         mbar_wait_sleep_bounded(&accum_bar, 0);
-      } else if (!PERSIST && !mbar_wait_sleep_bounded(&accum_bar, 0)) {
+      } else if (!mbar_wait_sleep_bounded(&accum_bar, 0)) {
         atomicOr(&flags, 2);
       }
     }
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint16_t *th = reinterpret_cast<uint16_t *>(smem + L.epi_off + q * 1024);
     griddep_wait();  // y may still be read by the previous kernel
     bool ok = true;
-    for (int it = 0; it < my_tiles && ok; ++it) {
+    for (int it = 0; it + 1 < my_tiles && ok; ++it) {  // all but the last tile
       const int ab = sp.dbl ? (it & 1) : 0, ause = sp.dbl ? (it >> 1) : it;
       if (!(ok = mbar_wait_sleep_bounded(&tfull_bar[ab], ause & 1))) break;
       tc_fence_after();
@@ -642,18 +643,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (!ok) atomicOr(&flags, 2);
   }
 
-  // ------------------------------------------------------------ end of a persistent CTA, or
-  // the epilogue of a one-tile CTA (all warps).  Only the MMA lane waits for a one-tile CTA's
-  // accumulator (above); every other thread parks in the hardware barrier below instead of
-  // polling, so the producers keep the issue slots.
+  // ------------------------------------------------------------ epilogue of the CTA's last
+  // (or only) tile, all warps.  Only the MMA lane waits for its accumulator (above); every other
+  // thread parks in the hardware barrier below instead of polling, so the producers keep the
+  // issue slots.  All 16 warps drain it (measured: a persistent CTA's last tile left to the four
+  // epilogue warps kept the CTA alive ~7,600 cycles after its last MMA at BM = 256).
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (PERSIST || !run) {
+  if (!run) {
     if (threadIdx.x == 0 && flags) atomicOr(err, flags);
   } else {
   griddep_wait();  // every storing thread waits for the previous kernel (a no-op once satisfied)
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bm;
+  const int n0 = tile_n0(my_tiles - 1), m0 = tile_m0(my_tiles - 1);
+  const uint32_t acol = sp.dbl ? (uint32_t)(((my_tiles - 1) & 1) * bm) : 0u;  // its accumulator
   // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (column-rows n) and the 16-column groups c of the
   // tile with c % kGroups == w / 4; a per-warp 2 KB transpose buffer in the (now idle) stage
   // memory turns each group into 16-byte stores of consecutive n.
@@ -768,27 +771,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
   } else {
-    uint16_t *th = reinterpret_cast<uint16_t *>(tb);
+    // rows (2i, 2i + 1) of a 16-column group as fp16 pairs, turned around as in the persistent
+    // epilogue: 16-byte stores of 8 consecutive n of two rows
+    uint32_t *tw = reinterpret_cast<uint32_t *>(tb);
     for (int c00 = 16 * third; c00 < bm; c00 += 3 * 16 * kGroups) {  // three 16-column groups per wait
       uint32_t v[3][16];
 #pragma unroll
       for (int b = 0; b < 3; ++b)
-        if (c00 + 16 * kGroups * b < bm) tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(c00 + 16 * kGroups * b), v[b]);
+        if (c00 + 16 * kGroups * b < bm)
+          tmem_ld16_async(tmem + ((uint32_t)(32 * quarter) << 16) + acol + (uint32_t)(c00 + 16 * kGroups * b), v[b]);
       tmem_wait_ld();
 #pragma unroll
       for (int b = 0; b < 3; ++b) {
         const int c0 = c00 + 16 * kGroups * b;
         if (c0 >= bm) break;
 #pragma unroll
-        for (int j2 = 0; j2 < 16; ++j2)
-          th[j2 * 32 + lane] = T::from_float(__uint_as_float(v[b][j2]));
+        for (int i = 0; i < 8; ++i)
+          tw[i * 32 + (lane ^ (4 * (i & 1)))] = T::pack2(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1]));
         __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {  // 64 pieces of 8 halves: (m = piece / 4, n = 8 * (piece % 4))
-          const int pc = lane + 32 * q, j2 = pc >> 2, nn = 8 * (pc & 3);
-          const int m = m0 + c0 + j2, n = nq + nn;
+        {
+          const int i = lane >> 2, nn = 8 * (lane & 3), sw = 4 * (i & 1);
+          const uint4 a = *reinterpret_cast<const uint4 *>(tw + i * 32 + nn + sw);
+          const uint4 c = *reinterpret_cast<const uint4 *>(tw + i * 32 + nn + (sw ^ 4));
+          uint4 lo, hi;
+          lo.x = __byte_perm(a.x, a.y, 0x5410);
+          lo.y = __byte_perm(a.z, a.w, 0x5410);
+          lo.z = __byte_perm(c.x, c.y, 0x5410);
+          lo.w = __byte_perm(c.z, c.w, 0x5410);
+          hi.x = __byte_perm(a.x, a.y, 0x7632);
+          hi.y = __byte_perm(a.z, a.w, 0x7632);
+          hi.z = __byte_perm(c.x, c.y, 0x7632);
+          hi.w = __byte_perm(c.z, c.w, 0x7632);
+          const int m = m0 + c0 + 2 * i, n = nq + nn;
           if (m < M && n < N && in_extent(y + (size_t)m * N + n, 16, y, yext, err))
-            *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = *reinterpret_cast<const uint4 *>(th + j2 * 32 + nn);
+            *reinterpret_cast<uint4 *>(y + (size_t)m * N + n) = lo;
+          if (m + 1 < M && n < N && in_extent(y + (size_t)(m + 1) * N + n, 16, y, yext, err))
+            *reinterpret_cast<uint4 *>(y + (size_t)(m + 1) * N + n) = hi;
         }
         __syncwarp();
       }
