@@ -63,7 +63,7 @@ def test_bf16_chunked_repack_is_byte_identical():
 GEMM_CASES = [
     ("square", 1), ("qkv", 1), ("gate_up", 1), ("down", 1),
     ("qkv", 3), ("gate_up", 16), ("down", 12), ("qkv", 8), ("gate_up", 8), ("qkv", 16), ("square", 10),
-    ("qkv", 32), ("gate_up", 33), ("down", 40),
+    ("qkv", 32), ("gate_up", 33), ("down", 40), ("down", 24), ("gate_up", 20),
     ("qkv", 512), ("gate_up", 512), ("down", 512), ("square", 129),
 ]
 
@@ -98,7 +98,7 @@ def test_gemm_bf16_small_ragged(K, N, g, M):
     assert_close_bf16(L.gemm(x), y64)
 
 
-@pytest.mark.parametrize("M", [1, 4, 8, 16, 32, 33, 130])
+@pytest.mark.parametrize("M", [1, 4, 8, 16, 20, 32, 33, 130])
 @pytest.mark.parametrize("g", [32, 128])
 def test_gemm_bf16_bit_exact_when_sums_are_exact(M, g):
     """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so both sides

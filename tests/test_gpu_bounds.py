@@ -40,12 +40,12 @@ def test_check_fires_in_the_debug_build_only():
 
 
 @pytest.mark.parametrize("K,N,g,Ms", [
-    (6656, 80, 32, (1, 3, 17, 40, 129)),       # N tail; decode, MB=2 decode, split-K, tensor core
-    (224, 200, 32, (5, 33)),                   # K % 128 != 0, N % 64 != 0
+    (6656, 80, 32, (1, 3, 12, 17, 40, 129)),   # N tail; decode at 1..16 rows, 17..32 rows, split-K, tensor core
+    (224, 200, 32, (5, 20, 33)),               # K % 128 != 0, N % 64 != 0
     (96, 8, 32, (2,)),                         # a single, partly filled chunk
     (4096, 264, 64, (16, 300)),                # long K decode; ragged tensor-core tiles
     (2048, 13312, 128, (1, 8, 300)),           # gate_up: lean decode, persistent tensor core
-    (6656, 2048, 128, (1, 24, 512)),           # down: 16-warp decode, split-K cluster
+    (6656, 2048, 128, (1, 24, 512)),           # down: 16-warp decode, 24 rows over a cluster, split-K cluster
 ])
 def test_gemm_clean_under_bounds_checks(checked, K, N, g, Ms):
     L = Layer(K, N, g, seed=K + N)

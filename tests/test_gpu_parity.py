@@ -263,7 +263,7 @@ def test_gemm_persistent_ragged_sampled(name, M, g):
 
 
 @pytest.mark.parametrize("g", [32, 64, 128])
-@pytest.mark.parametrize("M", [1, 3, 12, 17, 129])
+@pytest.mark.parametrize("M", [1, 3, 12, 17, 27, 129])
 @pytest.mark.parametrize("zeros", ["sym8", "uniform"])
 def test_gemm_edge_tail(g, M, zeros):
     K, N = SHAPES["tail80"]
@@ -283,7 +283,7 @@ def test_gemm_small_ragged(K, N, g, M):
     assert_close(L.gemm(x), y16)
 
 
-@pytest.mark.parametrize("M", [1, 4, 5, 8, 9, 12, 16, 17, 32, 33, 130])
+@pytest.mark.parametrize("M", [1, 4, 5, 8, 9, 12, 16, 17, 21, 32, 33, 130])
 @pytest.mark.parametrize("g", [32, 128])
 def test_gemm_bit_exact_when_sums_are_exact(M, g):
     """x in {-2..2} and s = 2^-8: every product and fp32 partial sum is exact, so the result must
@@ -310,7 +310,33 @@ def test_gemm_q_equal_z_gives_zero():
         assert torch.all(y == 0)
 
 
-@pytest.mark.parametrize("M", [1, 16, 512])
+@pytest.mark.parametrize("name,M,g", [("qkv", 17, 128), ("gate_up", 20, 128), ("down", 24, 128),
+                                     ("qkv", 32, 32), ("down", 31, 64), ("square", 29, 128)])
+def test_gemm_mid_rows_one_pass(name, M, g):
+    """17..32 rows: one pass over the weights, x staged once per CTA and K split over a cluster
+    of CTAs whose partials are added in rank order; down's 52 chunks leave a short last split,
+    and g = 32 / 64 scale each weight before the products."""
+    K, N = SHAPES[name]
+    L = Layer(K, N, g, seed=M)
+    x = inputs.make_x(M, K, seed=M)
+    _, y16 = L.ref(x)
+    assert_close(L.gemm(x), y16)
+    assert w4.last_device_error() == 0
+
+
+@pytest.mark.parametrize("K,N,g,M", [(160, 80, 32, 19), (224, 136, 32, 32), (6656, 80, 128, 25),
+                                     (4096, 264, 64, 18), (96, 8, 32, 23)])
+def test_gemm_mid_rows_ragged(K, N, g, M):
+    """17..32 rows with K not a multiple of 128, N not a multiple of 64, and fewer chunks than
+    splits would like."""
+    L = Layer(K, N, g, seed=K + M)
+    x = inputs.make_x(M, K, seed=M)
+    _, y16 = L.ref(x)
+    assert_close(L.gemm(x), y16)
+    assert w4.last_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 16, 24, 512])
 def test_gemm_deterministic(M):
     K, N = SHAPES["gate_up"]
     L = Layer(K, N, 128, seed=10)

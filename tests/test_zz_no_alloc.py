@@ -27,7 +27,7 @@ def _call(x, packed, M, N, K, g, y):
 # split-K shapes (scratch in use), shapes that need none, the decode path, the N = 80 tail
 CASES = [("down", 512, 128), ("qkv", 129, 128), ("qkv", 256, 128), ("qkv", 512, 128), ("square", 40, 128),
          ("gate_up", 512, 128), ("gate_up", 1, 128), ("tail80", 17, 32), ("qkv", 1, 128), ("qkv", 8, 128),
-         ("lm_head", 8, 128)]
+         ("lm_head", 8, 128), ("down", 24, 128), ("gate_up", 32, 64)]
 # the cases that split K: under the workspace reduction they run through the built-in scratch
 SPLIT = {("down", 512), ("qkv", 129), ("qkv", 256), ("square", 40)}
 

@@ -1,9 +1,11 @@
-// gemv.cu -- decode path of y = x . W for few rows of x (up to 16 per m-block).
+// gemv.cu -- decode path of y = x . W for few rows of x (M <= 32).
 //
-// Three kernels, picked by launch_gemv from M, K and the number of 16-column row-tiles:
-// gemv_kernel (any M, x in registers), gemv_small_kernel (M <= 8, x through a per-warp cp.async
-// ring, 64-80 registers so that 3-4 CTAs fit per SM) and gemv_stream_kernel (M <= 8, K <= 2048
-// and very wide layers: resident CTAs walking row-tile pairs).  What follows holds for all three.
+// Four kernels, picked by launch_gemv from M, K and the number of 16-column row-tiles:
+// gemv_kernel (M <= 16, x in registers), gemv_small_kernel (M <= 8, x through a per-warp cp.async
+// ring, 64-80 registers so that 3-4 CTAs fit per SM), gemv_stream_kernel (M <= 8, K <= 2048 and
+// very wide layers: resident CTAs walking row-tile pairs) and gemv_mid_kernel (17 <= M <= 32: x
+// staged once per CTA, K split over a cluster).
+// What follows holds for all four.
 //
 // Why a separate path: "single-stream decode reads every weight to emit one token, so bits
 // per weight set the token rate" (vllm-omni commit "Add cpu_int4, an asymmetric 4-bit weight
@@ -538,6 +540,175 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Mid-size decode, 17 <= M <= 32 rows of x (MB = 4; the kernel also takes MB = 2): one pass over
+// the weights, where gemv_kernel would take two 16-row passes, each warp fetching from L2 the x of
+// every chunk it takes (four to eight times the bytes of the weights it multiplies).  A CTA owns
+// one n-block (64 columns: its 4 warps take one row-tile each) over a range of chunks and stages
+// each chunk of x once in a shared-memory ring (cp.async, the swizzled layout of the lean kernel)
+// that all four warps read, so x costs twice the weights' bytes.  K is split over the S CTAs of
+// a thread-block cluster (grid: n-blocks x S); each leaves its fp32 partial in shared memory and
+// adds 1/S of the n-block's outputs over the S partials in rank order through distributed shared
+// memory, so y does not depend on timing.
+constexpr int kMidWarps = 4;      // one per row-tile of the n-block
+constexpr int kMidDepth = 4;      // chunks of weights in flight per warp (registers)
+constexpr int kMidSlots = 4;      // chunks of x staged in shared memory; equal to kMidDepth
+constexpr int kMidMaxSplits = 8;  // portable cluster size
+
+template <class T, int MB, bool FACTOR>
+__global__ void __launch_bounds__(32 * kMidWarps) gemv_mid_kernel(const uint16_t *__restrict__ x,
+                                                                 const uint8_t *__restrict__ packed, int M, int N,
+                                                                 int K, int g, int KT, int cps, int S,
+                                                                 uint16_t *__restrict__ y, int *err) {
+  constexpr int R = 8 * MB;             // rows of x per slot (zeros past M)
+  constexpr int kSlotBytes = R * 256;   // 128 k of fp16 per row
+  constexpr int kVals = MB * 4;         // accumulator values per lane
+  static_assert(kMidWarps * kVals * 32 * 4 <= kMidSlots * kSlotBytes, "partials fit in the x ring");
+  __shared__ __align__(16) uint8_t xs[kMidSlots * kSlotBytes];
+  __shared__ int bad;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r8 = lane >> 2, t = lane & 3;
+  const int b = blockIdx.x, z = blockIdx.y;  // n-block; split = rank in the cluster
+  const int c0 = z * cps, nch = max(0, min(KT, c0 + cps) - c0);
+  const int CB = chunk_bytes(g);
+  const uint8_t *body = packed + kHeaderBytes + ((size_t)b * KT + c0) * CB;
+  const long long pext = packed_extent(K, N, g), xext = 2LL * M * K, yext = 2LL * M * N;
+  int hdr_ok = 1;
+  if (threadIdx.x == 0) hdr_ok = header_ok<T>(packed, K, N, g, pext, err);
+
+  auto load_w = [&](Stage<1> &st, int j) {  // chunk c0 + j of row-tile `warp`
+    const uint8_t *ch = body + (size_t)j * CB;
+    const uint8_t *meta = ch + kCodeBytes + ((32 * t) / g) * kGroupMetaBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) st.code[0][h] = ld_w16(ch + (16 * warp + r8 + 8 * h) * kRowBytes + 16 * t, packed, pext, err);
+    st.scale[0] = ld_w4(meta + 2 * (8 * r8 + 2 * warp), packed, pext, err);
+    st.zero[0] = ld_w1(meta + kScaleBytes + 4 * r8 + warp, packed, pext, err);
+  };
+  // x rows 0..R-1 of chunk c0 + j into slot `slot`, by all threads (16-byte pieces)
+  auto load_x = [&](int slot, int j) {
+    const int k0 = (c0 + j) * kTileK;
+    uint8_t *dst = xs + slot * kSlotBytes;
+#pragma unroll
+    for (int i = 0; i < MB; ++i) {
+      const int p = (int)threadIdx.x + i * 32 * kMidWarps, m = p >> 4, q = p & 15;
+      const bool ok = m < M && k0 + 8 * q < K && in_extent(x + (size_t)m * K + k0 + 8 * q, 16, x, xext, err);
+      cp_async16_zfill(dst + m * 256 + 16 * xring_piece<true>(m, q), ok ? x + (size_t)m * K + k0 + 8 * q : x, ok);
+    }
+  };
+
+  Stage<1> st[kMidDepth];
+#pragma unroll
+  for (int d = 0; d < kMidDepth; ++d)
+    if (d < nch) load_w(st[d], d);
+  griddep_launch_dependents();
+  griddep_wait();  // x may be the previous kernel's output; y may still be read by it
+#pragma unroll
+  for (int d = 0; d < kMidSlots - 1; ++d) {
+    if (d < nch) load_x(d, d);
+    cp_async_commit();  // one group per chunk, possibly empty
+  }
+
+  float acc[MB][4];
+#pragma unroll
+  for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[mb][c] = 0.f;
+  const int xc = 16 * ((2 * (t >> 1)) | (r8 & 1));  // the lane's reads in the swizzled slot
+
+#pragma unroll 1
+  for (int j0 = 0; j0 < nch; j0 += kMidDepth) {
+#pragma unroll
+    for (int d = 0; d < kMidDepth; ++d) {
+      const int j = j0 + d;  // uniform over the CTA
+      if (j < nch) {
+        cp_async_wait_pending<kMidSlots - 2>();  // chunk j's x has landed (this thread's pieces)
+        __syncthreads();                          // ... every thread's; slot (j - 1) % kMidSlots is free
+        if (j + kMidSlots - 1 < nch) load_x((d + kMidSlots - 1) % kMidSlots, j + kMidSlots - 1);
+        cp_async_commit();
+        const uint8_t *xsl = xs + d * kSlotBytes + 64 * t;  // slot j % kMidSlots == d
+        Stage<1> &s = st[d];
+        const ZeroBias zb0 = T::zb(s.zero[0] & 0xFu), zb1 = T::zb((s.zero[0] >> 4) & 0xFu);
+        float dd[MB][4];
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dd[mb][e] = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t w0 = (w == 0) ? s.code[0][0].x : (w == 1) ? s.code[0][0].y : (w == 2) ? s.code[0][0].z : s.code[0][0].w;
+          const uint32_t w1 = (w == 0) ? s.code[0][1].x : (w == 1) ? s.code[0][1].y : (w == 2) ? s.code[0][1].z : s.code[0][1].w;
+          uint32_t v0[4], v1[4];
+          T::qz(w0, zb0, v0);
+          T::qz(w1, zb1, v1);
+          if (!FACTOR) {
+            const uint32_t s20 = (s.scale[0] & 0xFFFFu) * 0x00010001u, s21 = (s.scale[0] >> 16) * 0x00010001u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v0[e] = T::mul2(v0[e], s20);
+              v1[e] = T::mul2(v1[e], s21);
+            }
+          }
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            float *dst = FACTOR ? dd[mb] : acc[mb];
+            const uint4 xw = *reinterpret_cast<const uint4 *>(xsl + (8 * mb + r8) * 256 + ((16 * w) ^ xc));
+            T::mma16816(dst, v0[0], v1[0], v0[1], v1[1], xw.x, xw.y);  // k 8w + 0..3
+            T::mma16816(dst, v0[2], v1[2], v0[3], v1[3], xw.z, xw.w);  // k 8w + 4..7
+          }
+        }
+        if (FACTOR) {
+          const float f0 = T::to_float(s.scale[0] & 0xFFFFu);
+          const float f1 = T::to_float(s.scale[0] >> 16);
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            acc[mb][0] = fmaf(f0, dd[mb][0], acc[mb][0]);
+            acc[mb][1] = fmaf(f0, dd[mb][1], acc[mb][1]);
+            acc[mb][2] = fmaf(f1, dd[mb][2], acc[mb][2]);
+            acc[mb][3] = fmaf(f1, dd[mb][3], acc[mb][3]);
+          }
+        }
+        if (j + kMidDepth < nch) load_w(s, j + kMidDepth);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- reduction over the cluster
+  cp_async_wait_pending<0>();
+  __syncthreads();  // every warp is done with the x ring: it now holds the partials
+  float *red = reinterpret_cast<float *>(xs);  // [warp][kVals][32]
+#pragma unroll
+  for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) red[(warp * kVals + mb * 4 + c) * 32 + lane] = acc[mb][c];
+  if (threadIdx.x == 0) bad = !hdr_ok;  // the same verdict in every CTA: one packed buffer
+  if (S > 1) {
+    cluster_arrive();  // release: the partials are visible to the cluster
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
+  if (bad) {
+    if (z == 0 && threadIdx.x == 0) atomicOr(err, 1);
+  } else {
+    constexpr int E = kMidWarps * kVals * 32;
+    const int e1 = (z + 1) * E / S;
+    for (int e = z * E / S + (int)threadIdx.x; e < e1; e += 32 * kMidWarps) {
+      float v = 0.f;
+      for (int zz = 0; zz < S; ++zz) v += S > 1 ? ld_cluster_f32(mapa_shared(red + e, (uint32_t)zz)) : red[e];
+      const int ln = e & 31, vi = (e >> 5) % kVals, wp = e / (32 * kVals);
+      const int c = vi & 3, mb = vi >> 2;
+      const int n = b * kBlockN + 16 * wp + (ln >> 2) + 8 * (c >> 1);
+      const int m = 8 * mb + 2 * (ln & 3) + (c & 1);
+      if (m < M && n < N && in_extent(y + (size_t)m * N + n, 2, y, yext, err)) y[(size_t)m * N + n] = T::from_float(v);
+    }
+  }
+  if (S > 1) {
+    cluster_arrive();  // no CTA leaves while another still reads its partials
+    cluster_wait();
+  }
+}
+
 int sm_count() {
   static std::atomic<int> count[64];  // per device, 0 until looked up
   int dev = 0;
@@ -580,13 +751,13 @@ cudaError_t launch_variant(int tiles, int mblocks, int W, const uint16_t *x, con
 }
 
 template <class T, int RT>
-cudaError_t launch_rt(int tiles, int mblocks, int W, int MB, bool factor, const uint16_t *x, const uint8_t *p,
-                      int M, int N, int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
+cudaError_t launch_rt(int tiles, int W, int MB, bool factor, const uint16_t *x, const uint8_t *p, int M, int N,
+                      int K, int g, int KT, uint16_t *y, int *err, cudaStream_t stream) {
   if (MB == 1)
-    return factor ? launch_variant<T, RT, 1, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
-                  : launch_variant<T, RT, 1, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
-  return factor ? launch_variant<T, RT, 2, true>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream)
-                : launch_variant<T, RT, 2, false>(tiles, mblocks, W, x, p, M, N, K, g, KT, y, err, stream);
+    return factor ? launch_variant<T, RT, 1, true>(tiles, 1, W, x, p, M, N, K, g, KT, y, err, stream)
+                  : launch_variant<T, RT, 1, false>(tiles, 1, W, x, p, M, N, K, g, KT, y, err, stream);
+  return factor ? launch_variant<T, RT, 2, true>(tiles, 1, W, x, p, M, N, K, g, KT, y, err, stream)
+                : launch_variant<T, RT, 2, false>(tiles, 1, W, x, p, M, N, K, g, KT, y, err, stream);
 }
 
 template <class T>
@@ -666,17 +837,144 @@ cudaError_t launch_small(int tiles, bool factor, const uint16_t *x, const uint8_
                 : cudaLaunchKernelEx(&cfg, gemv_small_kernel<T, D, RT, false, false>, x, p, M, N, K, g, KT, y, err);
 }
 
+// Dynamic shared memory (unused) that holds a mid-size kernel to `per` CTAs per SM: more than
+// 1 / (per + 1) of the SM's shared memory with the static part and the per-CTA reservation.
+// The kernel's opt-in limit is set once, to the largest pad (per = 1), and never lowered, so
+// every pad stays launchable whatever order the launches come in (cached per kernel and device).
+template <class T, int MB, bool FACTOR>
+size_t mid_pad(int per) {
+  auto kernel = gemv_mid_kernel<T, MB, FACTOR>;
+  static std::atomic<int> state[64];  // 0: not looked up; 1: ready; -1: no pads
+  static long long per_sm[64], fixed[64];  // shared memory per SM; static part + reservation
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || per < 1) return 0;
+  int st = state[dev].load(std::memory_order_acquire);
+  if (!st) {
+    int sm = 0, reserved = 0;
+    cudaFuncAttributes fa = {};
+    cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    st = -1;
+    if (sm > 0 && cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
+      per_sm[dev] = sm;
+      fixed[dev] = (long long)fa.sharedSizeBytes + reserved;
+      const long long largest = ((sm / 2 + 1024 - fixed[dev] + 1023) / 1024) * 1024;
+      if (largest > 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)largest) == cudaSuccess)
+        st = 1;
+    }
+    cudaGetLastError();
+    state[dev].store(st, std::memory_order_release);
+  }
+  if (st < 0) return 0;
+  const long long need = per_sm[dev] / (per + 1) + 1024 - fixed[dev];
+  return need <= 0 ? 0 : (size_t)(((need + 1023) / 1024) * 1024);
+}
+
+// How many CTAs of a mid-size kernel fit per SM, and whether `nclusters` clusters of S of them,
+// held to `per` per SM, can be resident at once (cached per kernel, device, S and `per`).
+template <class T, int MB, bool FACTOR>
+int mid_fit(int S, int nclusters, int per = 0) {
+  auto kernel = gemv_mid_kernel<T, MB, FACTOR>;
+  static std::atomic<int> per_sm[64];                   // 0 until looked up, else value + 1
+  static std::atomic<int> clusters[64][kMidMaxSplits + 1][8];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || S < 1 || S > kMidMaxSplits || per < 0 || per >= 8) return 0;
+  if (nclusters <= 0) {  // the CTAs per SM
+    int v = per_sm[dev].load(std::memory_order_relaxed);
+    if (!v) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 32 * kMidWarps, 0) != cudaSuccess) n = 0;
+      cudaGetLastError();
+      v = (n > 0 ? n : 1) + 1;
+      per_sm[dev].store(v, std::memory_order_relaxed);
+    }
+    return v - 1;
+  }
+  int v = clusters[dev][S][per].load(std::memory_order_relaxed);
+  if (!v) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, S);
+    cfg.blockDim = dim3(32 * kMidWarps);
+    cfg.dynamicSmemBytes = per > 0 ? mid_pad<T, MB, FACTOR>(per) : 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = S;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+    cudaGetLastError();
+    v = n + 1;
+    clusters[dev][S][per].store(v, std::memory_order_relaxed);
+  }
+  return (v - 1) >= nclusters ? 1 : 0;
+}
+
+// Mid-size decode launch: n-blocks x S splits of K, S the largest count (at most 8, at most the
+// chunks) whose CTAs fit in one wave and whose clusters are all resident at once.
+template <class T, int MB, bool FACTOR>
+cudaError_t launch_mid(const uint16_t *x, const uint8_t *p, int M, int N, int K, int g, int KT, uint16_t *y,
+                       int *err, cudaStream_t stream) {
+  const int NB = num_nblocks(N);
+  const long wave = (long)mid_fit<T, MB, FACTOR>(1, 0) * sm_count();
+  int S = (int)std::max(1L, std::min<long>(kMidMaxSplits, wave / NB));
+  S = std::min(S, KT);
+  int cps = (KT + S - 1) / S;
+  S = (KT + cps - 1) / cps;  // no empty split
+  // The block scheduler fills an SM before it moves on: hold the CTAs to ceil(CTAs / SMs) per SM
+  // with unused dynamic shared memory, so that the grid spreads over all SMs.
+  const int fit = mid_fit<T, MB, FACTOR>(1, 0);
+  auto held = [&](int s) {
+    const int per = (int)(((long)NB * s + sm_count() - 1) / sm_count());
+    return per < fit ? per : 0;
+  };
+  while (S > 1 && !mid_fit<T, MB, FACTOR>(S, NB, held(S))) {
+    --S;
+    cps = (KT + S - 1) / S;
+    S = (KT + cps - 1) / cps;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(NB, S);
+  cfg.blockDim = dim3(32 * kMidWarps);
+  cfg.dynamicSmemBytes = held(S) > 0 ? mid_pad<T, MB, FACTOR>(held(S)) : 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (S > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = S;
+    attr[1].val.clusterDim.z = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemv_mid_kernel<T, MB, FACTOR>, x, p, M, N, K, g, KT, cps, S, y, err);
+}
+
 template <class T>
 cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, int K, int g, uint16_t *y,
                           int *err, cudaStream_t stream) {
   const int KT = num_ktiles(K);
-  const int MB = (M <= 8) ? 1 : 2;
-  const int mblocks = (M + 8 * MB - 1) / (8 * MB);
-  // Row-tiles of 16 columns that hold at least one column < N (N % 8 == 0).
-  const int tiles = (N + 15) / 16;
   const uint8_t *p = static_cast<const uint8_t *>(packed);
   const bool factor = (g == kTileK);
-  const long ctas1 = (long)tiles * mblocks;
+  // 17..32 rows: one pass over the weights, x shared by the CTA, K split over a cluster
+  // (measured against two 16-row passes of gemv_kernel: q_k_v M = 24 6.14 -> 5.12 us, gate_up
+  // M = 32 13.9 -> 12.55 us).  At 9..16 rows gemv_kernel's single pass stays faster (the same
+  // kernel with 16 rows: q_k_v 3.6 -> 4.1 us, gate_up 7.7 -> 9.2 us, down 6.9 either way).
+  if (M > 16)
+    return factor ? launch_mid<T, 4, true>(x, p, M, N, K, g, KT, y, err, stream)
+                  : launch_mid<T, 4, false>(x, p, M, N, K, g, KT, y, err, stream);
+  const int MB = (M <= 8) ? 1 : 2;
+  // Row-tiles of 16 columns that hold at least one column < N (N % 8 == 0).
+  const int tiles = (N + 15) / 16;
+  const long ctas1 = tiles;
   // Lean variant for M <= 8 unless K is long and the grid is small (then 16 warps per CTA win).
   const bool long_k = KT >= 32 && ctas1 <= sm_count();
   if (M <= kSmallRows && !long_k) {
@@ -699,8 +997,8 @@ cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, i
   const int sms = sm_count();
   const bool two = ctas1 >= (MB == 1 ? 4L : 1L) * sms;
   const int W = (ctas1 >= 4L * sms) ? 4 : (!two && long_k && MB == 1) ? 16 : 8;
-  if (two) return launch_rt<T, 2>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
-  return launch_rt<T, 1>(tiles, mblocks, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+  if (two) return launch_rt<T, 2>(tiles, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
+  return launch_rt<T, 1>(tiles, W, MB, factor, x, p, M, N, K, g, KT, y, err, stream);
 }
 
 }  // namespace
