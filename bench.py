@@ -429,16 +429,17 @@ def run_configs(args, w4, torch, dev, stream, layers, timed, hbm, bf16, peak_src
         return lambda: w4.gemm(x, p, M, N, K, G, y=y, workspace=ws, stream=stream)
 
     out = {}
-    M = 16
-    m16 = {}
-    for si, (name, K, N) in enumerate(DECODE_SHAPES):
-        x = torch.from_numpy(inputs.make_x(M, K, seed=16)).to(dev)
-        y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        ms = graph_time([gemm_call(x, lin[si][3], M, N, K, y) for lin in layers], min(500, max(20, args.steps // 20)))
-        b = alg_bytes(M, K, N)
-        m16[name] = {"us_per_launch": round(ms * 1e3, 3), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
-                     "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
-    out["decode_shapes_M16"] = m16
+    # 16 rows (gemv_kernel) and 32 rows (one pass of gemv_mid_kernel) through the step's shapes
+    for M in (16, 32):
+        mm = {}
+        for si, (name, K, N) in enumerate(DECODE_SHAPES):
+            x = torch.from_numpy(inputs.make_x(M, K, seed=16)).to(dev)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            ms = graph_time([gemm_call(x, lin[si][3], M, N, K, y) for lin in layers], min(500, max(20, args.steps // 20)))
+            b = alg_bytes(M, K, N)
+            mm[name] = {"us_per_launch": round(ms * 1e3, 3), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                        "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+        out["decode_shapes_M%d" % M] = mm
     K, N = inputs.SHAPES["square"]
     sq = []
     for i in range(16):
