@@ -845,7 +845,7 @@ template <class T, int MB, bool FACTOR>
 size_t mid_pad(int per) {
   auto kernel = gemv_mid_kernel<T, MB, FACTOR>;
   static std::atomic<int> state[64];  // 0: not looked up; 1: ready; -1: no pads
-  static long long per_sm[64], fixed[64];  // shared memory per SM; static part + reservation
+  static std::atomic<long long> per_sm[64], fixed[64];  // shared memory per SM; static part + reservation
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || per < 1) return 0;
@@ -857,9 +857,10 @@ size_t mid_pad(int per) {
     cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     st = -1;
     if (sm > 0 && cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
-      per_sm[dev] = sm;
-      fixed[dev] = (long long)fa.sharedSizeBytes + reserved;
-      const long long largest = ((sm / 2 + 1024 - fixed[dev] + 1023) / 1024) * 1024;
+      const long long fx = (long long)fa.sharedSizeBytes + reserved;
+      per_sm[dev].store(sm, std::memory_order_relaxed);
+      fixed[dev].store(fx, std::memory_order_relaxed);
+      const long long largest = ((sm / 2 + 1024 - fx + 1023) / 1024) * 1024;
       if (largest > 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)largest) == cudaSuccess)
         st = 1;
     }
@@ -867,7 +868,8 @@ size_t mid_pad(int per) {
     state[dev].store(st, std::memory_order_release);
   }
   if (st < 0) return 0;
-  const long long need = per_sm[dev] / (per + 1) + 1024 - fixed[dev];
+  const long long need = per_sm[dev].load(std::memory_order_relaxed) / (per + 1) + 1024 -
+                         fixed[dev].load(std::memory_order_relaxed);
   return need <= 0 ? 0 : (size_t)(((need + 1023) / 1024) * 1024);
 }
 
