@@ -56,7 +56,7 @@ SCRIPT = textwrap.dedent(r'''
                         if (i + tid) % 2:
                             continue
                         packed, x, K, N = layers[key]
-                        y = w4.gemm(x, packed, key[1], N, K, 128, stream=s)
+                        y = w4.gemm(x, packed, key[1], N, K, 128, stream=s)  # a workspace per stream
                         results[(tid, rep, key)] = y
             s.synchronize()
         except Exception as e:  # reported by the main thread

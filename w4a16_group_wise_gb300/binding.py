@@ -8,6 +8,7 @@ fallback: if the shared library is missing or fails to load, every call raises.
 import contextlib
 import ctypes
 import os
+import threading
 
 import torch
 
@@ -179,17 +180,24 @@ def repack_chunk(qweight_c, qzeros_c, scales_c, K, N, g, n0, n1, packed, stream=
 
 
 _workspaces = {}
+_workspaces_lock = threading.Lock()
 
 
-def default_workspace(nbytes, device):
-    """A zero-filled workspace of at least `nbytes` bytes, cached per device.  Every completed
-    call leaves it zero-filled, so it is reused; calls on different streams that may overlap
-    need workspaces of their own."""
-    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
-    ws = _workspaces.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
+def default_workspace(nbytes, device, stream=None):
+    """A zero-filled workspace of at least `nbytes` bytes, cached per device and stream.  Every
+    completed call leaves it zero-filled, so calls on one stream reuse it; calls on different
+    streams get different workspaces, so they may overlap.  (Calls that share a stream run one
+    after the other: a call touches the workspace only after the previous kernel in the stream
+    has finished.)"""
+    index = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    if stream is None:
+        stream = torch.cuda.current_stream(index)
+    key = (index, stream.cuda_stream)
+    with _workspaces_lock:
+        ws = _workspaces.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            _workspaces[key] = ws
     return ws
 
 
@@ -201,7 +209,7 @@ def gemm(x, packed, M, N, K, g, y=None, workspace=None, stream=None):
     _dev(y, x.dtype, "y")
     need = workspace_bytes(M, N, K, g)
     if need and workspace is None:
-        workspace = default_workspace(need, x.device)
+        workspace = default_workspace(need, x.device, stream)
     ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     fn = "w4a16_gemm" + _SUFFIX[x.dtype]

@@ -735,7 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
              (atomicAdd(&sp.counters[tile], 1) == sp.splits - 1);
     __syncthreads();
     if (!last) {
-      fl = 0;  // errors are reported by the last CTA of the tile
+      if (fl && threadIdx.x == 0) atomicOr(err, fl);  // the last CTA adds what it finds
+      fl = 0;
     } else {
       __threadfence();
       if (threadIdx.x == 0) sp.counters[tile] = 0;  // ready for the next call
