@@ -374,6 +374,14 @@ def test_header_mismatch_is_reported_and_nothing_written():
     assert w4.last_device_error() == 0
     bad = L.packed.clone()
     bad[0] ^= 0xFF                                       # corrupt the magic
+    # the lean decode kernel, the 16-row kernel, the one-pass mid-size kernel (a cluster of K
+    # splits that all see the bad header), the tensor-core kernel
+    for Mb in (1, 12, 24, 40):
+        xb = torch.from_numpy(inputs.make_x(Mb, K)).to(dev())
+        yb = torch.full((Mb, N), 7.0, dtype=torch.float16, device=dev())
+        w4.gemm(xb, bad, Mb, N, K, g, y=yb)
+        assert w4.last_device_error() == w4.binding.ERR_DEVICE, Mb
+        assert torch.all(yb == 7.0), Mb
     x = torch.from_numpy(inputs.make_x(2, K)).to(dev())
     y = torch.full((2, N), 7.0, dtype=torch.float16, device=dev())
     w4.gemm(x, bad, 2, N, K, g, y=y)
