@@ -26,9 +26,40 @@ __device__ __forceinline__ int awq_slot_of_col(int c) { return (c & 1) ? 4 + (c 
 __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 * (p % 2) + p / 8; }
 
 constexpr int kRepackBlocks = 4;  // n-blocks per CTA: 32 AWQ words = 128 contiguous bytes of a row
+constexpr int kRepackThreads = 256;
+
+// Transpose an 8 x 8 matrix of nibbles held as 8 words (row i = R[i], column p = bits 4p..4p+3):
+// afterwards R[p] holds, in nibble i, what R[i] held in nibble p.  Three rounds of masked swaps
+// exchange 4-, 8- and 16-bit blocks between rows 1, 2 and 4 apart.
+__device__ __forceinline__ void nibble_transpose8(uint32_t (&R)[8]) {
+#pragma unroll
+  for (int a = 0; a < 8; a += 2) {
+    const uint32_t t = ((R[a] >> 4) ^ R[a + 1]) & 0x0F0F0F0Fu;
+    R[a + 1] ^= t;
+    R[a] ^= t << 4;
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {  // rows (0,2) (1,3) (4,6) (5,7)
+    const int a = (h & 1) + 4 * (h >> 1);
+    const uint32_t t = ((R[a] >> 8) ^ R[a + 2]) & 0x00FF00FFu;
+    R[a + 2] ^= t;
+    R[a] ^= t << 8;
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const uint32_t t = ((R[a] >> 16) ^ R[a + 4]) & 0x0000FFFFu;
+    R[a + 4] ^= t;
+    R[a] ^= t << 16;
+  }
+}
+
+// XOR applied to the code-word index w of column-row r of n-block bl in the shared output tile, so
+// that the transposing threads' stores (32 lanes: 4 n-blocks x 8 words of 8 columns) and the
+// copy-out's reads both hit distinct banks.
+__device__ __forceinline__ int out_swizzle(int bl, int r) { return ((r >> 5) & 1) | (bl << 1); }
 
 // One CTA: kRepackBlocks consecutive n-blocks b0 + 4 blockIdx.x + bl (those below b1) of k-tile t.
-__global__ void __launch_bounds__(256) repack_kernel(
+__global__ void __launch_bounds__(kRepackThreads) repack_kernel(
     const int32_t *__restrict__ qweight, int64_t ldq, const int32_t *__restrict__ qzeros,
     int64_t ldz, const uint16_t *__restrict__ scales, int64_t lds, int K, int N, int g, int gsrc, int dtype,
     int n0, int n1, int b0, int b1, int KT, uint8_t *__restrict__ packed, int *err) {
@@ -66,11 +97,32 @@ __global__ void __launch_bounds__(256) repack_kernel(
   __shared__ uint32_t in[kTileK][kW + 1];
   __shared__ uint32_t out[kRepackBlocks][kBlockN][17];  // code words per n-block (row stride 17)
   __shared__ uint32_t zin[4][kW];                       // [group of the chunk][AWQ zero word]
-  for (int i = threadIdx.x; i < kTileK * kW; i += blockDim.x) {
-    const int kk = i / kW, c = i % kW;
+  constexpr int kLoads = kTileK * kW / kRepackThreads;  // words per thread, all requested at once
+  uint32_t v[kLoads];
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int i = (int)threadIdx.x + u * kRepackThreads, kk = i / kW, c = i % kW;
     const int k = kb + kk, b = bfirst + c / 8, n = b * kBlockN + 8 * (c % 8);
     const int32_t *src = qweight + (int64_t)k * ldq + (n - n0) / 8;
-    in[kk][c] = (k < K && b < b1 && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
+    v[u] = (k < K && b < b1 && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
+  }
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int i = (int)threadIdx.x + u * kRepackThreads;
+    in[i / kW][i % kW] = v[u];
+  }
+  // the scales of the CTA's n-blocks, requested with the codes (at most 4 groups per chunk)
+  __shared__ uint16_t sin[kRepackBlocks][4][kBlockN];  // [n-block][group of the chunk][column]
+#pragma unroll
+  for (int u = 0; u < (kRepackBlocks * 4 * kBlockN) / kRepackThreads; ++u) {
+    const int i = (int)threadIdx.x + u * kRepackThreads;
+    const int bl = i / (4 * kBlockN), l = (i / kBlockN) % 4, r = i % kBlockN;
+    if (l < gpc) {
+      const int b = bfirst + bl, grp = t * gpc + l, n = b * kBlockN + r;
+      const int sg = (grp * g) / gsrc;
+      const uint16_t *src = scales + (int64_t)sg * lds + (n - n0);
+      sin[bl][l][r] = (b < b1 && grp < G && n < N && in_extent(src, 2, scales, sext, err)) ? __ldg(src) : (uint16_t)0;
+    }
   }
   if (threadIdx.x < gpc * kW) {
     const int l = threadIdx.x / kW, c = threadIdx.x % kW;
@@ -81,15 +133,22 @@ __global__ void __launch_bounds__(256) repack_kernel(
   }
   __syncthreads();
 
-  // Codes: row r (column 64 b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  Threads take r
-  // fastest, so a warp reads 4 distinct words per step (the rest are broadcasts).
-  for (int i = threadIdx.x; i < kRepackBlocks * kBlockN * 16; i += blockDim.x) {
-    const int r = i & (kBlockN - 1), w = (i >> 6) & 15, bl = i >> 10;
-    const int c = 8 * bl + (r >> 3), sh = 4 * awq_slot_of_col(r & 7);
-    uint32_t o = 0;
+  // Codes: row r (column 64 b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  A thread takes
+  // the 8 AWQ words of rows kb + 8w + slot_k(j) (j = 0..7) of word-column c -- 8 k x 8 columns of
+  // nibbles -- and transposes them in registers: word p is then the code word of the column in
+  // AWQ slot p.  Threads take c fastest, so the reads of a row are consecutive words.
+  for (int i = threadIdx.x; i < kW * 16; i += blockDim.x) {
+    const int c = i % kW, w = i / kW;
+    uint32_t R[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o |= ((in[8 * w + slot_k(j)][c] >> sh) & 0xFu) << (4 * j);
-    out[bl][r][w] = o;
+    for (int j = 0; j < 8; ++j) R[j] = in[8 * w + slot_k(j)][c];
+    nibble_transpose8(R);
+    const int bl = c >> 3;
+#pragma unroll
+    for (int col = 0; col < 8; ++col) {
+      const int r = 8 * (c & 7) + col;
+      out[bl][r][w ^ out_swizzle(bl, r)] = R[awq_slot_of_col(col)];
+    }
   }
   __syncthreads();
 
@@ -100,19 +159,15 @@ __global__ void __launch_bounds__(256) repack_kernel(
     // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
     uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
     for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x)
-      if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[bl][i >> 4][i & 15];
+      if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[bl][i >> 4][(i & 15) ^ out_swizzle(bl, i >> 4)];
 
     // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
     // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
     // source tensors (gsrc == g, or gsrc == K for one group over all of K).
     for (int i = threadIdx.x; i < gpc * kBlockN; i += blockDim.x) {
-      const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r, read in order
-      const int grp = t * gpc + l, n = b * kBlockN + r;
-      const int sg = (grp * g) / gsrc;
-      const uint16_t *src = scales + (int64_t)sg * lds + (n - n0);
-      const uint16_t sv = (grp < G && n < N && in_extent(src, 2, scales, sext, err)) ? *src : (uint16_t)0;
+      const int l = i / kBlockN, r = i % kBlockN;  // source column 64b + r
       uint16_t *dst = reinterpret_cast<uint16_t *>(chunk + kCodeBytes + l * kGroupMetaBytes) + meta_pos(r);
-      if (in_extent(dst, 2, packed, pext, err)) *dst = sv;
+      if (in_extent(dst, 2, packed, pext, err)) *dst = sin[bl][l][r];
     }
     if (threadIdx.x < gpc * 8) {
       const int l = threadIdx.x >> 3, wi = threadIdx.x & 7;
@@ -137,7 +192,7 @@ cudaError_t launch_repack(const int32_t *qweight, int64_t ldq, const int32_t *qz
   int b1 = (n1 + kBlockN - 1) / kBlockN;
   int KT = num_ktiles(K);
   dim3 grid((b1 - b0 + kRepackBlocks - 1) / kRepackBlocks, KT);
-  repack_kernel<<<grid, 256, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0, n1,
+  repack_kernel<<<grid, kRepackThreads, 0, stream>>>(qweight, ldq, qzeros, ldz, scales, lds, K, N, g, gsrc, dtype, n0, n1,
                                           b0, b1, KT, static_cast<uint8_t *>(packed), err);
   return cudaGetLastError();
 }
