@@ -29,8 +29,9 @@ constexpr int kRepackBlocks = 4;  // n-blocks per CTA: 32 AWQ words = 128 contig
 constexpr int kRepackThreads = 256;
 
 // Transpose an 8 x 8 matrix of nibbles held as 8 words (row i = R[i], column p = bits 4p..4p+3):
-// afterwards R[p] holds, in nibble i, what R[i] held in nibble p.  Three rounds of masked swaps
-// exchange 4-, 8- and 16-bit blocks between rows 1, 2 and 4 apart.
+// afterwards R[p] holds, in nibble i, what R[i] held in nibble p.  Three rounds exchange 4-, 8-
+// and 16-bit blocks between rows 1, 2 and 4 apart: masked swaps for the nibbles, byte permutes
+// for the bytes and half-words.
 __device__ __forceinline__ void nibble_transpose8(uint32_t (&R)[8]) {
 #pragma unroll
   for (int a = 0; a < 8; a += 2) {
@@ -39,17 +40,17 @@ __device__ __forceinline__ void nibble_transpose8(uint32_t (&R)[8]) {
     R[a] ^= t << 4;
   }
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {  // rows (0,2) (1,3) (4,6) (5,7)
+  for (int h = 0; h < 4; ++h) {  // rows (0,2) (1,3) (4,6) (5,7): even bytes of a with those of a + 2
     const int a = (h & 1) + 4 * (h >> 1);
-    const uint32_t t = ((R[a] >> 8) ^ R[a + 2]) & 0x00FF00FFu;
-    R[a + 2] ^= t;
-    R[a] ^= t << 8;
+    const uint32_t x = R[a], y = R[a + 2];
+    R[a] = __byte_perm(x, y, 0x6240);
+    R[a + 2] = __byte_perm(x, y, 0x7351);
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const uint32_t t = ((R[a] >> 16) ^ R[a + 4]) & 0x0000FFFFu;
-    R[a + 4] ^= t;
-    R[a] ^= t << 16;
+  for (int a = 0; a < 4; ++a) {  // low half-words of a with those of a + 4
+    const uint32_t x = R[a], y = R[a + 4];
+    R[a] = __byte_perm(x, y, 0x5410);
+    R[a + 4] = __byte_perm(x, y, 0x7632);
   }
 }
 
@@ -158,8 +159,11 @@ __global__ void __launch_bounds__(kRepackThreads) repack_kernel(
     uint8_t *chunk = packed + kHeaderBytes + ((size_t)b * KT + t) * CB;
     // the 4 KB of codes in layout order, a warp storing 128 contiguous bytes at a time
     uint32_t *codes = reinterpret_cast<uint32_t *>(chunk);
-    for (int i = threadIdx.x; i < kBlockN * 16; i += blockDim.x)
+#pragma unroll
+    for (int u = 0; u < kBlockN * 16 / kRepackThreads; ++u) {
+      const int i = (int)threadIdx.x + u * kRepackThreads;
       if (in_extent(codes + i, 4, packed, pext, err)) codes[i] = out[bl][i >> 4][(i & 15) ^ out_swizzle(bl, i >> 4)];
+    }
 
     // Meta: per group of the chunk, 64 scales and 64 zero nibbles in lane order.  Layout group
     // grp covers rows [grp g, grp g + g); its scales and zeros are row (grp g) / gsrc of the
