@@ -25,8 +25,9 @@
 //    which frees the stage when they complete.
 // Without a K split the CTAs are persistent (one per SM, walking the tiles) and warps 12..15
 // read each finished accumulator back (tcgen05.ld), round to fp16 and store y while the
-// producers run ahead on the next tile; with a K split every CTA has one tile and all warps
-// take part in adding the partial tiles.  Every wait is bounded: on a timeout the kernel
+// producers run ahead on the next tile; a CTA's last tile is drained by all 16 warps.  With a K
+// split every CTA has one tile and all warps take part in adding the partial tiles.  The two
+// cases run as separate instances of the kernel (PERSIST).  Every wait is bounded: on a timeout the kernel
 // records an error, drains, frees tensor memory and skips the store.
 // A bf16 layer runs the same kernel with T = Bf16 (dq.cuh): bf16 weights bf16((q - z) * s), x
 // loaded as bf16 by the TMA, the bf16 operand type in the instruction descriptor, y rounded to
