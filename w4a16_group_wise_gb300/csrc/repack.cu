@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kRepackThreads) repack_kernel(
   // n-block read as 0): a warp reads one row's 128 contiguous bytes.  The row stride of 33 words
   // keeps the transposition's reads free of bank conflicts.  Also the zero words of the groups.
   constexpr int kW = 8 * kRepackBlocks;  // AWQ words of a row in this CTA
+  static_assert((kTileK * kW) % kRepackThreads == 0 && (kBlockN * 16) % kRepackThreads == 0 &&
+                    (kRepackBlocks * 4 * kBlockN) % kRepackThreads == 0,
+                "the unrolled loads, scale loads and code copy-out give every thread the same count");
   const int gpc = kTileK / g;            // groups per chunk
   const int G = K / g;
   __shared__ uint32_t in[kTileK][kW + 1];
