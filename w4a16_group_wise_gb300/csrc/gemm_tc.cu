@@ -227,12 +227,13 @@ struct SplitPlan {
 };
 
 // Cluster split-K reduction of one CTA's pieces [e0, e1) of the tile (float4 pieces, 32 per row
-// m): the S CTAs' fp32 partials (`part` in every CTA's shared memory), read through distributed
-// shared memory, added in rank order -- the workspace reduction's order -- and stored as y; U
-// pieces per thread in flight.
+// m): the S CTAs' fp32 partials (`part` in every CTA's shared memory), the other CTAs' read
+// through distributed shared memory and this CTA's own (rank `me`) straight from its shared
+// memory, added in rank order -- the workspace reduction's order -- and stored as y; U pieces per
+// thread in flight.
 template <class T, int S, int U>
-__device__ __forceinline__ void cluster_reduce(const float *part, int e0, int e1, int m0, int n0, int M, int N,
-                                               uint16_t *__restrict__ y, int *err) {
+__device__ __forceinline__ void cluster_reduce(const float *part, int me, int e0, int e1, int m0, int n0, int M,
+                                               int N, uint16_t *__restrict__ y, int *err) {
   uint32_t base[S];
 #pragma unroll
   for (int z = 0; z < S; ++z) base[z] = mapa_shared(part, (uint32_t)z);
@@ -244,7 +245,9 @@ __device__ __forceinline__ void cluster_reduce(const float *part, int e0, int e1
       if (eu < e1) {
         const uint32_t off = (uint32_t)((eu >> 5) * kBN + 4 * (eu & 31)) * 4u;
 #pragma unroll
-        for (int z = 0; z < S; ++z) v[u][z] = ld_cluster_f4(base[z] + off);
+        for (int z = 0; z < S; ++z)
+          v[u][z] = z == me ? *reinterpret_cast<const float4 *>(reinterpret_cast<const uint8_t *>(part) + off)
+                            : ld_cluster_f4(base[z] + off);
       }
     }
 #pragma unroll
@@ -694,17 +697,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       if (blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, any);
     } else {
       const int E = bm * (kBN / 4);  // float4 pieces of the tile, 32 per row m
+      const int me = (int)blockIdx.z;  // rank in the cluster (1 x 1 x splits)
       const int e0 = (int)((long)blockIdx.z * E / sp.splits), e1 = (int)((long)(blockIdx.z + 1) * E / sp.splits);
       // pieces in flight per thread: 16 loads whatever the split count (measured: two pieces per
       // thread, four round trips at two splits, took ~5,600 cycles per 256-row tile)
       switch (sp.splits) {
-        case 2: cluster_reduce<T, 2, 8>(part, e0, e1, m0, n0, M, N, y, err); break;
-        case 3: cluster_reduce<T, 3, 5>(part, e0, e1, m0, n0, M, N, y, err); break;
-        case 4: cluster_reduce<T, 4, 4>(part, e0, e1, m0, n0, M, N, y, err); break;
-        case 5: cluster_reduce<T, 5, 3>(part, e0, e1, m0, n0, M, N, y, err); break;
-        case 6: cluster_reduce<T, 6, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
-        case 7: cluster_reduce<T, 7, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
-        default: cluster_reduce<T, 8, 2>(part, e0, e1, m0, n0, M, N, y, err); break;
+        case 2: cluster_reduce<T, 2, 8>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        case 3: cluster_reduce<T, 3, 5>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        case 4: cluster_reduce<T, 4, 4>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        case 5: cluster_reduce<T, 5, 3>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        case 6: cluster_reduce<T, 6, 2>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        case 7: cluster_reduce<T, 7, 2>(part, me, e0, e1, m0, n0, M, N, y, err); break;
+        default: cluster_reduce<T, 8, 2>(part, me, e0, e1, m0, n0, M, N, y, err); break;
       }
     }
     cluster_arrive();  // no CTA leaves while another still reads its partial

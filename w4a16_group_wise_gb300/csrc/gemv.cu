@@ -548,8 +548,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
 // each chunk of x once in a shared-memory ring (cp.async, the swizzled layout of the lean kernel)
 // that all four warps read, so x costs twice the weights' bytes.  K is split over the S CTAs of
 // a thread-block cluster (grid: n-blocks x S); each leaves its fp32 partial in shared memory and
-// adds 1/S of the n-block's outputs over the S partials in rank order through distributed shared
-// memory, so y does not depend on timing.
+// adds 1/S of the n-block's outputs over the S partials in rank order (its own from its shared
+// memory, the others' through distributed shared memory), so y does not depend on timing.
 constexpr int kMidWarps = 4;      // one per row-tile of the n-block
 constexpr int kMidDepth = 4;      // chunks of weights in flight per warp (registers)
 constexpr int kMidSlots = 4;      // chunks of x staged in shared memory; equal to kMidDepth
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(32 * kMidWarps) gemv_mid_kernel(const uint16_t
     const int e1 = (z + 1) * E / S;
     for (int e = z * E / S + (int)threadIdx.x; e < e1; e += 32 * kMidWarps) {
       float v = 0.f;
-      for (int zz = 0; zz < S; ++zz) v += S > 1 ? ld_cluster_f32(mapa_shared(red + e, (uint32_t)zz)) : red[e];
+      for (int zz = 0; zz < S; ++zz) v += zz == z ? red[e] : ld_cluster_f32(mapa_shared(red + e, (uint32_t)zz));
       const int ln = e & 31, vi = (e >> 5) % kVals, wp = e / (32 * kVals);
       const int c = vi & 3, mb = vi >> 2;
       const int n = b * kBlockN + 16 * wp + (ln >> 2) + 8 * (c >> 1);
