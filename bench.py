@@ -44,8 +44,8 @@ METRIC = "W4A16 GEMM effective HBM GB/s at M=1 (decoder-layer linears q_k_v/gate
 # captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch each of q_k_v, gate_up
 # and down at M=1, summarised under profiles/), keyed by the sha256 of the kernel source they
 # were taken on; reported as null whenever that source has changed since.
-TRAFFIC = {"source_sha256": "2f85102902aa8d1dab980bedeaa7208d0be91d3ad2715d23e1eaf7bd55829eb2",
-           "bytes_per_launch": (3299584 + 14200320 + 7120128) // 3}
+TRAFFIC = {"source_sha256": "fd75e56cfa2c1f18b3b9bc76f2ab6de870dbb528eb1801b08063662249be8e2a",
+           "bytes_per_launch": (3299328 + 14200576 + 7119616) // 3}
 
 
 def max_over_ranks(ms, world, device):
