@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 3) gemv_stream_kernel(
 }
 
 // ---------------------------------------------------------------------------------------------
-// Mid-size decode, 17 <= M <= 32 rows of x (MB = 4; the kernel also takes MB = 2): one pass over
+// Mid-size decode, 17 <= M <= 32 rows of x (MB = 3 up to 24 rows, else 4): one pass over
 // the weights, where gemv_kernel would take two 16-row passes, each warp fetching from L2 the x of
 // every chunk it takes (four to eight times the bytes of the weights it multiplies).  A CTA owns
 // one n-block (64 columns: its 4 warps take one row-tile each) over a range of chunks and stages
@@ -970,9 +970,12 @@ cudaError_t launch_gemv_t(const uint16_t *x, const void *packed, int M, int N, i
   // (measured against two 16-row passes of gemv_kernel: q_k_v M = 24 6.14 -> 5.12 us, gate_up
   // M = 32 13.9 -> 12.55 us).  At 9..16 rows gemv_kernel's single pass stays faster (the same
   // kernel with 16 rows: q_k_v 3.6 -> 4.1 us, gate_up 7.7 -> 9.2 us, down 6.9 either way).
-  if (M > 16)
+  if (M > 24)
     return factor ? launch_mid<T, 4, true>(x, p, M, N, K, g, KT, y, err, stream)
                   : launch_mid<T, 4, false>(x, p, M, N, K, g, KT, y, err, stream);
+  if (M > 16)  // 24 rows of x per slot (measured against 32: q_k_v M = 24 5.1 -> 4.6 us, gate_up M = 17 12.4 -> 10.5 us)
+    return factor ? launch_mid<T, 3, true>(x, p, M, N, K, g, KT, y, err, stream)
+                  : launch_mid<T, 3, false>(x, p, M, N, K, g, KT, y, err, stream);
   const int MB = (M <= 8) ? 1 : 2;
   // Row-tiles of 16 columns that hold at least one column < N (N % 8 == 0).
   const int tiles = (N + 15) / 16;
