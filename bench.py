@@ -812,7 +812,8 @@ def workload_config(n_launches=3 * LAYERS, packed_mb=None, world=1):
 
 def run_profile_case(spec):
     """A small fixed case for ncu: [OP:]SHAPE:M with OP gemm (default; M rows of x), repack,
-    dequant or embed (M token ids); 2 warm-up launches, then 3 launches (capture with -s 2 -c 3)."""
+    dequant, embed (M token ids) or convert (AWQ -> standard packing; M unused); 2 warm-up
+    launches, then 3 launches (capture with -s 2 -c 3)."""
     import torch
     import __graft_entry__
     import w4a16_group_wise_gb300 as w4
@@ -844,6 +845,9 @@ def run_profile_case(spec):
         out = torch.empty((M, K), dtype=torch.float16, device=dev)
         for _ in range(5):
             w4.embed(ids, packed, K, N, G, out=out)
+    elif op == "convert":
+        for _ in range(5):
+            w4.awq_to_standard(qw, qz, K, N, G)
     else:
         raise ValueError("unknown profile op %r" % op)
     torch.cuda.synchronize()
