@@ -15,6 +15,7 @@
 #include "bounds.cuh"
 #include "kernels.h"
 #include "layout.cuh"
+#include "nibble.cuh"
 
 namespace w4a16 {
 namespace {
@@ -27,32 +28,6 @@ __device__ __forceinline__ int meta_row(int p) { return 16 * ((p % 8) / 2) + 8 *
 
 constexpr int kRepackBlocks = 4;  // n-blocks per CTA: 32 AWQ words = 128 contiguous bytes of a row
 constexpr int kRepackThreads = 256;
-
-// Transpose an 8 x 8 matrix of nibbles held as 8 words (row i = R[i], column p = bits 4p..4p+3):
-// afterwards R[p] holds, in nibble i, what R[i] held in nibble p.  Three rounds exchange 4-, 8-
-// and 16-bit blocks between rows 1, 2 and 4 apart: masked swaps for the nibbles, byte permutes
-// for the bytes and half-words.
-__device__ __forceinline__ void nibble_transpose8(uint32_t (&R)[8]) {
-#pragma unroll
-  for (int a = 0; a < 8; a += 2) {
-    const uint32_t t = ((R[a] >> 4) ^ R[a + 1]) & 0x0F0F0F0Fu;
-    R[a + 1] ^= t;
-    R[a] ^= t << 4;
-  }
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {  // rows (0,2) (1,3) (4,6) (5,7): even bytes of a with those of a + 2
-    const int a = (h & 1) + 4 * (h >> 1);
-    const uint32_t x = R[a], y = R[a + 2];
-    R[a] = __byte_perm(x, y, 0x6240);
-    R[a + 2] = __byte_perm(x, y, 0x7351);
-  }
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {  // low half-words of a with those of a + 4
-    const uint32_t x = R[a], y = R[a + 4];
-    R[a] = __byte_perm(x, y, 0x5410);
-    R[a + 4] = __byte_perm(x, y, 0x7632);
-  }
-}
 
 // XOR applied to the code-word index w of column-row r of n-block bl in the shared output tile, so
 // that the transposing threads' stores (32 lanes: 4 n-blocks x 8 words of 8 columns) and the
