@@ -64,31 +64,33 @@ __global__ void __launch_bounds__(kRepackThreads) repack_kernel(
       reinterpret_cast<uint32_t *>(packed)[threadIdx.x] = v;
   }
 
-  // The 128 x 32 AWQ words of the CTA's n-blocks (rows past K, columns past N or past the last
-  // n-block read as 0): a warp reads one row's 128 contiguous bytes.  The row stride of 33 words
-  // keeps the transposition's reads free of bank conflicts.  Also the zero words of the groups.
+  // The code words.  Row r of n-block b (column 64 b + r), word w holds k = kb + 8w + slot_k(j) in
+  // slot j.  A thread takes kUnits (word-column c, k-octet w) units of the CTA's 32 x 16, c
+  // fastest, and loads the 8 AWQ words of rows kb + 8w + slot_k(j) (j = 0..7) of word-column c --
+  // 8 k x 8 columns of nibbles -- straight into registers (a warp's load is one row's 128
+  // contiguous bytes; rows past K, columns past N or past the last n-block read as 0), every word
+  // requested before any is used.  Transposed in registers, word p is the code word of the column
+  // in AWQ slot p.
   constexpr int kW = 8 * kRepackBlocks;  // AWQ words of a row in this CTA
-  static_assert((kTileK * kW) % kRepackThreads == 0 && (kBlockN * 16) % kRepackThreads == 0 &&
+  constexpr int kUnits = kW * 16 / kRepackThreads;
+  static_assert((kW * 16) % kRepackThreads == 0 && (kBlockN * 16) % kRepackThreads == 0 &&
                     (kRepackBlocks * 4 * kBlockN) % kRepackThreads == 0,
                 "the unrolled loads, scale loads and code copy-out give every thread the same count");
   const int gpc = kTileK / g;            // groups per chunk
   const int G = K / g;
-  __shared__ uint32_t in[kTileK][kW + 1];
   __shared__ uint32_t out[kRepackBlocks][kBlockN][17];  // code words per n-block (row stride 17)
   __shared__ uint32_t zin[4][kW];                       // [group of the chunk][AWQ zero word]
-  constexpr int kLoads = kTileK * kW / kRepackThreads;  // words per thread, all requested at once
-  uint32_t v[kLoads];
+  uint32_t R[kUnits][8];
 #pragma unroll
-  for (int u = 0; u < kLoads; ++u) {
-    const int i = (int)threadIdx.x + u * kRepackThreads, kk = i / kW, c = i % kW;
-    const int k = kb + kk, b = bfirst + c / 8, n = b * kBlockN + 8 * (c % 8);
-    const int32_t *src = qweight + (int64_t)k * ldq + (n - n0) / 8;
-    v[u] = (k < K && b < b1 && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
-  }
+  for (int u = 0; u < kUnits; ++u) {
+    const int i = (int)threadIdx.x + u * kRepackThreads, c = i % kW, w = i / kW;
+    const int b = bfirst + c / 8, n = b * kBlockN + 8 * (c % 8);
 #pragma unroll
-  for (int u = 0; u < kLoads; ++u) {
-    const int i = (int)threadIdx.x + u * kRepackThreads;
-    in[i / kW][i % kW] = v[u];
+    for (int j = 0; j < 8; ++j) {
+      const int k = kb + 8 * w + slot_k(j);
+      const int32_t *src = qweight + (int64_t)k * ldq + (n - n0) / 8;
+      R[u][j] = (k < K && b < b1 && n < N && in_extent(src, 4, qweight, qext, err)) ? (uint32_t)__ldg(src) : 0u;
+    }
   }
   // the scales of the CTA's n-blocks, requested with the codes (at most 4 groups per chunk)
   __shared__ uint16_t sin[kRepackBlocks][4][kBlockN];  // [n-block][group of the chunk][column]
@@ -110,23 +112,15 @@ __global__ void __launch_bounds__(kRepackThreads) repack_kernel(
     const int32_t *src = qzeros + (int64_t)sg * ldz + (n - n0) / 8;
     zin[l][c] = (grp < G && b < b1 && n < N && in_extent(src, 4, qzeros, zext, err)) ? (uint32_t)__ldg(src) : 0u;
   }
-  __syncthreads();
-
-  // Codes: row r (column 64 b + r), word w holds k = kb + 8w + slot_k(j) in slot j.  A thread takes
-  // the 8 AWQ words of rows kb + 8w + slot_k(j) (j = 0..7) of word-column c -- 8 k x 8 columns of
-  // nibbles -- and transposes them in registers: word p is then the code word of the column in
-  // AWQ slot p.  Threads take c fastest, so the reads of a row are consecutive words.
-  for (int i = threadIdx.x; i < kW * 16; i += blockDim.x) {
-    const int c = i % kW, w = i / kW;
-    uint32_t R[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) R[j] = in[8 * w + slot_k(j)][c];
-    nibble_transpose8(R);
+  for (int u = 0; u < kUnits; ++u) {
+    const int i = (int)threadIdx.x + u * kRepackThreads, c = i % kW, w = i / kW;
+    nibble_transpose8(R[u]);
     const int bl = c >> 3;
 #pragma unroll
     for (int col = 0; col < 8; ++col) {
       const int r = 8 * (c & 7) + col;
-      out[bl][r][w ^ out_swizzle(bl, r)] = R[awq_slot_of_col(col)];
+      out[bl][r][w ^ out_swizzle(bl, r)] = R[u][awq_slot_of_col(col)];
     }
   }
   __syncthreads();
