@@ -492,7 +492,7 @@ def run_embed(args, w4, torch, dev, stream, timed, hbm, peak_src, T=4096):
     def conv():
         with torch.cuda.stream(stream):
             w4.awq_to_standard(qw, qz, K, N, G, stream=stream)
-    ms_conv = timed(conv, 10) / 10
+    ms_conv = timed(conv, 50) / 50
     conv_bytes = 2 * (qw.numel() + qz.numel()) * 4
     conv_gbs = conv_bytes / (ms_conv * 1e-3) / 1e9
     convert = {"metric": "AWQ -> standard repacking GB/s (%dx%d LM head tensors, read + written)" % (K, N),
