@@ -299,6 +299,28 @@ def test_gemm_bit_exact_when_sums_are_exact(M, g):
     assert np.array_equal(y, y16)
 
 
+@pytest.mark.parametrize("N,K,M,g", [(30000, 2048, 1, 128), (30000, 2048, 4, 128), (30000, 2048, 8, 32),
+                                     (13312, 2048, 512, 128), (13312, 2048, 777, 64)])
+def test_gemm_bit_exact_when_sums_are_exact_wide(N, K, M, g):
+    """The exact-sum pin above on the paths its 192-column layer does not reach: the streaming
+    decode (more than 1824 row-tiles: resident CTAs walking row-tile pairs) and the persistent
+    tensor-core path (gate_up at M = 512 and 777: several tiles per CTA, the last one drained by
+    all warps).  x in {-2..2} and s = 2^-8 keep every product and fp32 partial sum exact, so the
+    sampled outputs (the last columns included) must equal the oracle's bit for bit."""
+    L = Layer(K, N, g, seed=M + N)
+    L.scales_bits = np.full_like(L.scales_bits, 0x1C00)          # 2^-8
+    L.d_scales = torch.from_numpy(L.scales_bits.view(np.float16)).to(dev())
+    L.packed = w4.repack(L.d_qweight, L.d_qzeros, L.d_scales, K, N, g)
+    xi = np.random.default_rng(M + 1).integers(-2, 3, size=(M, K)).astype(np.float16)
+    y = L.gemm(xi).cpu().numpy().view(np.uint16)
+    assert w4.last_device_error() == 0
+    rng = np.random.default_rng(N + M)
+    mi = rng.integers(0, M, 4096)
+    ni = np.concatenate([rng.integers(0, N, 4096 - 64), np.arange(N - 64, N)])
+    ref = oracle.linear_sampled(xi.view(np.uint16), L.qweight, L.qzeros, L.scales_bits, K, N, g, mi, ni)
+    assert np.array_equal(y[mi, ni], oracle.double_to_half_bits(ref))
+
+
 def test_gemm_q_equal_z_gives_zero():
     K, N, g = 1024, 256, 64
     L = Layer(K, N, g, seed=9)
