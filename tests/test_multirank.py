@@ -127,3 +127,18 @@ def test_column_slices_edge_cases():
     assert shard.column_slices(2056, 2) == [(0, 1024), (1024, 2056)]
     with pytest.raises(ValueError):
         shard.column_slices(0, 2)
+
+
+def test_timed_graphs_span_more_than_l2():
+    """bench.py's one-shape timing graphs cycle through at least L2_SPAN bytes of weights (more than
+    the 129 MB L2): the buffers given first, then copies of them in turn, each in memory of its own."""
+    import torch
+    import bench
+    assert bench.L2_SPAN > 129e6
+    base = [torch.full((3268864,), i, dtype=torch.uint8) for i in range(8)]  # eight q_k_v-sized buffers
+    bufs = bench.over_l2(base)
+    total = sum(b.numel() * b.element_size() for b in bufs)
+    assert total >= bench.L2_SPAN and total - bufs[-1].numel() < bench.L2_SPAN  # no copy beyond the span
+    assert len(bufs) == 49 and all(a is b for a, b in zip(bufs, base))
+    assert len({b.data_ptr() for b in bufs}) == len(bufs)
+    assert all(torch.equal(bufs[i], base[i % 8]) for i in range(len(bufs)))
