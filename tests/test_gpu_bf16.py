@@ -113,6 +113,28 @@ def test_gemm_bf16_bit_exact_when_sums_are_exact(M, g):
     assert np.array_equal(device_bits(L.gemm(xi)), yb)
 
 
+@pytest.mark.parametrize("N,K,M,g", [(30000, 2048, 1, 128), (30000, 2048, 8, 32), (13312, 2048, 512, 128)])
+def test_gemm_bf16_bit_exact_when_sums_are_exact_wide(N, K, M, g):
+    """The wide exact-sum pin of the fp16 suite for a bf16 layer: the streaming decode (30000
+    columns) and the persistent tensor-core path (gate_up at M = 512).  x in {-2..2} and s = 2^-8
+    are exact in fp16 and bf16 alike, so the exact sums are those of the oracle's sampled product
+    over the same values, rounded once to bf16; the sampled outputs must match bit for bit."""
+    L = Layer(K, N, g, seed=M + N, dtype="bf16")
+    L.scales_bits = np.full_like(L.scales_bits, 0x3B80)          # 2^-8 in bf16
+    L.d_scales = bits_to_device(L.scales_bits, torch.bfloat16)
+    L.packed = w4.repack(L.d_qweight, L.d_qzeros, L.d_scales, K, N, g)
+    xi_int = np.random.default_rng(M + 2).integers(-2, 3, size=(M, K))
+    y = device_bits(L.gemm(inputs.bf16_bits(xi_int)))
+    assert w4.last_device_error() == 0
+    rng = np.random.default_rng(N + M + 1)
+    mi = rng.integers(0, M, 4096)
+    ni = np.concatenate([rng.integers(0, N, 4096 - 64), np.arange(N - 64, N)])
+    s16 = np.full_like(L.scales_bits, 0x1C00)                    # the same 2^-8 in fp16
+    ref = oracle.linear_sampled(xi_int.astype(np.float16).view(np.uint16), L.qweight, L.qzeros, s16, K, N, g,
+                                mi, ni)
+    assert np.array_equal(y[mi, ni], oracle.double_to_bf16_bits(ref))
+
+
 @pytest.mark.parametrize("M", [1, 512])
 def test_gemm_bf16_deterministic(M):
     K, N = SHAPES["gate_up"]
